@@ -1,0 +1,300 @@
+"""KV-outer block-sparse attention over a paged KV cache, for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libsa.so`` (``include/sa.h``).  The
+functions carry the same names as the C entry points and do argument
+marshalling only: every step of the method runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.
+
+The three steps (crate alice-llm 2.0.0, module sparse_attention):
+
+* :func:`sa_build_index` - CSR index keyed by (kv head, sparse block)
+  (``types.rs``, KvOuterIndex);
+* :func:`sa_forward` - per-edge partials o, m, l (``forward.rs``,
+  kvouter_forward);
+* :func:`sa_combine` - log-sum-exp merge per (query, q-head);
+* :func:`sa_attention` - the three on one stream without a host sync.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _native
+from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE,
+                      STATUS_NAMES)
+
+__all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index", "sa_forward",
+           "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
+           "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE"]
+
+
+class SAError(RuntimeError):
+    """A non-OK sa_status returned by the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        self.kind = STATUS_NAMES.get(self.code, f"UNKNOWN({code})")
+        text = _native.load().sa_status_string(self.code).decode()
+        super().__init__(f"{where}: {self.kind} ({text})")
+
+
+def _check(code: int, where: str) -> None:
+    if code != _native.SA_OK:
+        raise SAError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _host_i64(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _require(t, dtype, name, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def sa_status_string(code: int) -> str:
+    return _native.load().sa_status_string(int(code)).decode()
+
+
+def sa_version() -> str:
+    return _native.load().sa_version().decode()
+
+
+def sa_index_query_sizes(tq, hkv, topk, batch, max_pages, block_size, page_size) -> dict:
+    s = _native.SaIndexSizes()
+    _check(_native.load().sa_index_query_sizes(tq, hkv, topk, batch, max_pages, block_size,
+                                               page_size, ctypes.byref(s)),
+           "sa_index_query_sizes")
+    return {name: getattr(s, name) for name, _ in s._fields_}
+
+
+@dataclass
+class Index:
+    """Device arrays of one KV-outer index plus the C struct that points at them."""
+
+    sel_slots: torch.Tensor
+    sel_offsets: torch.Tensor
+    num_sel: torch.Tensor
+    edge_head_base: torch.Tensor
+    edges: torch.Tensor
+    inv: torch.Tensor
+    splits: torch.Tensor
+    totals: torch.Tensor
+    workspace: torch.Tensor
+    sizes: dict
+    c: _native.SaIndex
+
+    @property
+    def device(self):
+        return self.totals.device
+
+    def to_host(self) -> dict:
+        """Copies of the index arrays, shaped and trimmed like the oracle's."""
+        c = self.c
+        tot = self.totals.cpu().numpy()
+        E, S, U = int(tot[0]), int(tot[1]), int(tot[2])
+        hkv, nbs, tq, topk = c.hkv, c.nbs, c.tq, c.topk
+        return {
+            "sel_slots": self.sel_slots[: hkv * nbs].cpu().numpy().reshape(hkv, nbs),
+            "sel_offsets": self.sel_offsets.cpu().numpy().reshape(hkv, nbs + 1),
+            "num_sel": self.num_sel.cpu().numpy(),
+            "edge_head_base": self.edge_head_base.cpu().numpy(),
+            "edges": self.edges.view(-1, 2)[:E].cpu().numpy(),
+            "inv": self.inv.cpu().numpy().reshape(hkv, tq, topk),
+            "splits": self.splits.view(-1, 4)[:S].cpu().numpy(),
+            "n_units": U, "status": int(tot[3]),
+        }
+
+
+def allocate_index(tq, hkv, topk, batch, max_pages, block_size, page_size, device) -> Index:
+    """Allocate (with torch) every array an index over these sizes needs."""
+    s = sa_index_query_sizes(tq, hkv, topk, batch, max_pages, block_size, page_size)
+    dev = torch.device(device)
+    i32 = dict(dtype=torch.int32, device=dev)
+    i64 = dict(dtype=torch.int64, device=dev)
+    ws_words = (s["workspace_bytes"] + 255) // 8 + 32
+    idx = Index(
+        sel_slots=torch.empty(max(s["sel_slots"], 1), **i32),
+        sel_offsets=torch.empty(max(s["sel_offsets"], 1), **i32),
+        num_sel=torch.empty(max(s["num_sel"], 1), **i32),
+        edge_head_base=torch.empty(max(s["edge_head_base"], 1), **i64),
+        edges=torch.empty(max(s["edges"], 4), **i32),
+        inv=torch.empty(max(s["inv"], 1), **i32),
+        splits=torch.empty(max(s["splits"], 4), **i32),
+        totals=torch.zeros(max(s["totals"], 4), **i64),
+        workspace=torch.empty(ws_words, **i64),
+        sizes=s,
+        c=_native.SaIndex(),
+    )
+    c = idx.c
+    c.sel_slots = idx.sel_slots.data_ptr()
+    c.sel_offsets = idx.sel_offsets.data_ptr()
+    c.num_sel = idx.num_sel.data_ptr()
+    c.edge_head_base = idx.edge_head_base.data_ptr()
+    c.edges = idx.edges.data_ptr()
+    c.inv = idx.inv.data_ptr()
+    c.splits = idx.splits.data_ptr()
+    c.totals = idx.totals.data_ptr()
+    base = idx.workspace.data_ptr()
+    aligned = (base + 255) & ~255
+    c.workspace = aligned
+    c.workspace_bytes = idx.workspace.numel() * 8 - (aligned - base)
+    return idx
+
+
+def sa_build_index(selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, max_pages,
+                   block_size, page_size, split_edges=0, index: Index | None = None,
+                   stream=None) -> Index:
+    """Step 1.  ``selected`` [tq, hkv, topk] int32 (device), ``cu_seqlens_q_host``
+    the host copy (numpy / CPU tensor) of ``cu_seqlens_q`` [B+1] int64 (device),
+    ``used_kv_lens`` [B] int32 (device) or None."""
+    _require(selected, torch.int32, "selected")
+    dev = selected.device
+    tq, hkv, topk = (int(x) for x in selected.shape)
+    cu_h = _host_i64(cu_seqlens_q_host)
+    _require(cu_seqlens_q, torch.int64, "cu_seqlens_q", dev)
+    batch = cu_h.size - 1
+    if used_kv_lens is not None:
+        _require(used_kv_lens, torch.int32, "used_kv_lens", dev)
+    if index is None:
+        index = allocate_index(tq, hkv, topk, max(batch, 1), max_pages, block_size, page_size,
+                               dev)
+    _check(_native.load().sa_build_index(
+        _ptr(selected), tq, hkv, topk, cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q),
+        batch, _ptr(used_kv_lens), max_pages, block_size, page_size, split_edges,
+        ctypes.byref(index.c), _stream(stream, dev)), "sa_build_index")
+    return index
+
+
+def _kv_dtype(k):
+    if k.dtype == torch.float32:
+        return DTYPE_F32
+    if k.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"k_pages/v_pages must be float32 or bfloat16, got {k.dtype}")
+
+
+def partial_rows(index: Index, hq: int) -> int:
+    """Row capacity of the partial buffers: tq * hkv * topk * qhead."""
+    c = index.c
+    return max(c.tq * c.hkv * c.topk * (hq // c.hkv), 1)
+
+
+def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, used_kv_lens, hq,
+               hkv, head_dim, block_size, page_size, softmax_scale, causal, o_partial=None,
+               m_partial=None, l_partial=None, path=PATH_AUTO, stream=None):
+    """Step 2.  Returns (o_partial, m_partial, l_partial); the first
+    totals[0] * qhead rows are valid."""
+    _require(q, torch.float32, "q")
+    dev = q.device
+    kvd = _kv_dtype(k_pages)
+    _require(k_pages, k_pages.dtype, "k_pages", dev)
+    _require(v_pages, k_pages.dtype, "v_pages", dev)
+    _require(block_tables, torch.int32, "block_tables", dev)
+    _require(cu_seqlens_q, torch.int64, "cu_seqlens_q", dev)
+    if used_kv_lens is not None:
+        _require(used_kv_lens, torch.int32, "used_kv_lens", dev)
+    page_elems = hkv * page_size * head_dim
+    num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
+    rows = partial_rows(index, hq) if hkv > 0 and hq % max(hkv, 1) == 0 else 1
+    if o_partial is None:
+        o_partial = torch.empty((rows, head_dim), dtype=torch.float32, device=dev)
+    if m_partial is None:
+        m_partial = torch.empty(rows, dtype=torch.float32, device=dev)
+    if l_partial is None:
+        l_partial = torch.empty(rows, dtype=torch.float32, device=dev)
+    _check(_native.load().sa_forward(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(index.c),
+        _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), hq, hkv, head_dim,
+        block_size, page_size, softmax_scale, int(bool(causal)), _ptr(o_partial),
+        _ptr(m_partial), _ptr(l_partial), path, _stream(stream, dev)), "sa_forward")
+    return o_partial, m_partial, l_partial
+
+
+def sa_combine(index: Index, o_partial, m_partial, l_partial, hq, head_dim, out=None, lse=None,
+               with_lse=True, stream=None):
+    """Step 3.  Returns (out [tq, hq, d], lse [tq, hq] or None)."""
+    dev = o_partial.device
+    tq = index.c.tq
+    if out is None:
+        out = torch.empty((tq, hq, head_dim), dtype=torch.float32, device=dev)
+    if lse is None and with_lse:
+        lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
+    _check(_native.load().sa_combine(ctypes.byref(index.c), _ptr(o_partial), _ptr(m_partial),
+                                     _ptr(l_partial), hq, head_dim, _ptr(out), _ptr(lse),
+                                     _stream(stream, dev)), "sa_combine")
+    return out, lse
+
+
+def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens,
+                 block_tables, hq, hkv, head_dim, block_size, page_size, softmax_scale, causal,
+                 split_edges=0, index: Index | None = None, partials=None, out=None, lse=None,
+                 with_lse=True, path=PATH_AUTO, stream=None):
+    """Steps 1-3 in one call.  Returns (out, lse, index, (o, m, l)).  Pass
+    ``index`` / ``partials`` / ``out`` back in to reuse their memory."""
+    _require(q, torch.float32, "q")
+    dev = q.device
+    kvd = _kv_dtype(k_pages)
+    tq, hkv_s, topk = (int(x) for x in selected.shape)
+    cu_h = _host_i64(cu_seqlens_q_host)
+    batch = cu_h.size - 1
+    max_pages = int(block_tables.shape[1])
+    if index is None:
+        index = allocate_index(tq, hkv_s, topk, max(batch, 1), max_pages, block_size, page_size,
+                               dev)
+    rows = max(tq * hkv_s * topk * (hq // max(hkv_s, 1)), 1)
+    if partials is None:
+        partials = (torch.empty((rows, head_dim), dtype=torch.float32, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev))
+    if out is None:
+        out = torch.empty((tq, hq, head_dim), dtype=torch.float32, device=dev)
+    if lse is None and with_lse:
+        lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
+    page_elems = hkv * page_size * head_dim
+    num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
+    o, m, l = partials
+    _check(_native.load().sa_attention(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, _ptr(selected), tq, topk,
+        cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), batch, _ptr(used_kv_lens),
+        _ptr(block_tables), max_pages, hq, hkv, head_dim, block_size, page_size, softmax_scale,
+        int(bool(causal)), split_edges, ctypes.byref(index.c), _ptr(o), _ptr(m), _ptr(l),
+        _ptr(out), _ptr(lse), path, _stream(stream, dev)), "sa_attention")
+    return out, lse, index, partials
+
+
+def sa_get_status(index: Index, stream=None) -> int:
+    """Synchronise and return the device status code (0 = OK)."""
+    return int(_native.load().sa_get_status(ctypes.byref(index.c),
+                                            _stream(stream, index.device)))
+
+
+def sa_clear_status(index: Index, stream=None) -> None:
+    _check(_native.load().sa_clear_status(ctypes.byref(index.c), _stream(stream, index.device)),
+           "sa_clear_status")

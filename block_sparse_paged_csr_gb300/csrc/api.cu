@@ -1,0 +1,288 @@
+// C ABI of libsa (declared in include/sa.h): argument checks in the order of
+// kvouter_forward's "argument sanity" (forward.rs) and of the error enum
+// (types.rs), then kernel launches on the caller's stream.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "sa.h"
+#include "sa_common.cuh"
+
+namespace sa {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace sa
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sa_status validate_cu_host(const int64_t* cu, int32_t batch) {
+  if (cu == nullptr || batch < 1 || cu[0] != 0) return SA_ERR_CU_SEQLENS;
+  for (int32_t b = 1; b <= batch; ++b)
+    if (cu[b] < cu[b - 1]) return SA_ERR_CU_SEQLENS;
+  return SA_OK;
+}
+
+sa_status check_geometry(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32_t max_pages,
+                         int32_t block_size, int32_t page_size, int64_t* msb_out,
+                         int64_t* nbs_out) {
+  if (block_size <= 0 || page_size <= 0 || block_size % page_size != 0) return SA_ERR_BLOCK_PAGE;
+  if (tq == 0 || hkv == 0 || topk == 0) return SA_ERR_EMPTY;
+  if (tq < 0 || hkv < 0 || topk < 0 || max_pages < 0) return SA_ERR_SHAPE;
+  if (batch < 1) return SA_ERR_CU_SEQLENS;
+  const int64_t ppb = block_size / page_size;
+  const int64_t msb = max_pages / ppb;
+  const int64_t n = tq * hkv * static_cast<int64_t>(topk);
+  if (n >= (int64_t{1} << 31) || msb > sa::kMaxMsb || msb * block_size >= (int64_t{1} << 31))
+    return SA_ERR_UNSUPPORTED;
+  const int64_t nbs = batch * msb;
+  if (static_cast<int64_t>(hkv) * (nbs + 1) >= (int64_t{1} << 31)) return SA_ERR_UNSUPPORTED;
+  *msb_out = msb;
+  *nbs_out = nbs;
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sa_status_string(sa_status status) {
+  switch (status) {
+    case SA_OK: return "ok";
+    case SA_ERR_HEAD_COUNT: return "Hq must be a positive multiple of Hkv";
+    case SA_ERR_BLOCK_PAGE: return "block_size must be a positive multiple of page_size";
+    case SA_ERR_CU_SEQLENS: return "cu_seqlens_q invalid (empty or not monotonic)";
+    case SA_ERR_SHAPE: return "shape mismatch";
+    case SA_ERR_SELECTED_RANGE: return "selected block id out of range [-1, msb)";
+    case SA_ERR_HEAD_DIM: return "head dim mismatch across q/k_cache/v_cache";
+    case SA_ERR_EMPTY: return "empty input";
+    case SA_ERR_CUDA: return "CUDA runtime error";
+    case SA_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case SA_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+    case SA_ERR_INVALID_ARGUMENT: return "invalid argument (null, misaligned or too small)";
+  }
+  return "unknown status";
+}
+
+const char* sa_version(void) { return "sa-gb300 0.1 (sm_103a)"; }
+
+sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t batch,
+                               int32_t max_pages, int32_t block_size, int32_t page_size,
+                               sa_index_sizes* out) {
+  if (out == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  int64_t msb = 0, nbs = 0;
+  const sa_status st =
+      check_geometry(tq, hkv, topk, batch, max_pages, block_size, page_size, &msb, &nbs);
+  if (st != SA_OK) return st;
+  const int64_t n = tq * hkv * static_cast<int64_t>(topk);
+  std::memset(out, 0, sizeof(*out));
+  out->msb = msb;
+  out->nbs = nbs;
+  out->sel_slots = nbs > 0 ? static_cast<int64_t>(hkv) * nbs : 1;
+  out->sel_offsets = static_cast<int64_t>(hkv) * (nbs + 1);
+  out->num_sel = hkv;
+  out->edge_head_base = static_cast<int64_t>(hkv) + 1;
+  out->edges = 2 * n;
+  out->inv = n;
+  out->splits = 4 * n;
+  out->totals = 4;
+  out->workspace_bytes = sa::workspace_layout(hkv, batch).total;
+  return SA_OK;
+}
+
+sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32_t topk,
+                         const int64_t* cu_seqlens_q_host, const int64_t* cu_seqlens_q,
+                         int32_t batch, const int32_t* used_kv_lens, int32_t max_pages,
+                         int32_t block_size, int32_t page_size, int32_t split_edges,
+                         sa_index* idx, void* stream) {
+  if (block_size <= 0 || page_size <= 0 || block_size % page_size != 0) return SA_ERR_BLOCK_PAGE;
+  if (tq == 0 || hkv == 0 || topk == 0) return SA_ERR_EMPTY;
+  sa_status st = validate_cu_host(cu_seqlens_q_host, batch);
+  if (st != SA_OK) return st;
+  if (cu_seqlens_q_host[batch] != tq) return SA_ERR_SHAPE;
+  int64_t msb = 0, nbs = 0;
+  st = check_geometry(tq, hkv, topk, batch, max_pages, block_size, page_size, &msb, &nbs);
+  if (st != SA_OK) return st;
+  if (split_edges < 0) return SA_ERR_INVALID_ARGUMENT;
+  if (idx == nullptr || selected == nullptr || cu_seqlens_q == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (!idx->sel_slots || !idx->sel_offsets || !idx->num_sel || !idx->edge_head_base ||
+      !idx->edges || !idx->inv || !idx->splits || !idx->totals || !idx->workspace)
+    return SA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(idx->splits) || !aligned16(idx->edges) ||
+      (reinterpret_cast<uintptr_t>(idx->workspace) & 255u) != 0)
+    return SA_ERR_INVALID_ARGUMENT;
+  const sa::WorkspaceLayout lay = sa::workspace_layout(hkv, batch);
+  if (idx->workspace_bytes < lay.total) return SA_ERR_INVALID_ARGUMENT;
+
+  idx->tq = tq;
+  idx->hkv = hkv;
+  idx->topk = topk;
+  idx->batch = batch;
+  idx->max_pages = max_pages;
+  idx->block_size = block_size;
+  idx->page_size = page_size;
+  idx->pages_per_block = block_size / page_size;
+  idx->msb = static_cast<int32_t>(msb);
+  idx->nbs = nbs;
+  idx->split_edges = split_edges;
+
+  sa::IndexArgs a{};
+  a.selected = selected;
+  a.cu = cu_seqlens_q;
+  a.used = used_kv_lens;
+  a.tq = tq;
+  a.hkv = hkv;
+  a.topk = topk;
+  a.batch = batch;
+  a.msb = static_cast<int32_t>(msb);
+  a.block_size = block_size;
+  a.split_edges = split_edges;
+  a.nbs = nbs;
+  a.idx = *idx;
+  const cudaError_t err = sa::launch_build_index(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, int64_t num_pages,
+                     sa_dtype kv_dtype, const sa_index* idx, const int32_t* block_tables,
+                     const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, int32_t hq,
+                     int32_t hkv, int32_t head_dim, int32_t block_size, int32_t page_size,
+                     float softmax_scale, int32_t causal, float* o_partial, float* m_partial,
+                     float* l_partial, sa_path path, void* stream) {
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
+  if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
+    return SA_ERR_BLOCK_PAGE;
+  if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (idx->hkv != hkv || idx->pages_per_block != block_size / page_size ||
+      idx->block_size != block_size || idx->page_size != page_size)
+    return SA_ERR_SHAPE;
+  if (num_pages < 0) return SA_ERR_SHAPE;
+  if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
+  const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
+  if (path == SA_PATH_TENSOR_CORE) return SA_ERR_UNSUPPORTED;
+  if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE) return SA_ERR_INVALID_ARGUMENT;
+  if (!sa::forward_cc_supported(head_dim, block_size, kv_bf16)) return SA_ERR_UNSUPPORTED;
+  if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
+      !l_partial)
+    return SA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o_partial))
+    return SA_ERR_INVALID_ARGUMENT;
+
+  sa::ForwardArgs a{};
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.num_pages = num_pages;
+  a.kv_bf16 = kv_bf16;
+  a.block_tables = block_tables;
+  a.cu = cu_seqlens_q;
+  a.used = used_kv_lens;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.qhead = hq / hkv;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.page_size = page_size;
+  a.pages_per_block = block_size / page_size;
+  a.max_pages = idx->max_pages;
+  a.msb = idx->msb;
+  a.nbs = idx->nbs;
+  a.scale = softmax_scale;
+  a.causal = causal != 0;
+  a.sel_slots = idx->sel_slots;
+  a.edges = idx->edges;
+  a.splits = idx->splits;
+  a.totals = idx->totals;
+  a.max_splits = idx->tq * idx->hkv * static_cast<int64_t>(idx->topk);
+  a.o_partial = o_partial;
+  a.m_partial = m_partial;
+  a.l_partial = l_partial;
+  if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
+  const cudaError_t err = sa::launch_forward_cc(a, static_cast<cudaStream_t>(stream));
+  if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m_partial,
+                     const float* l_partial, int32_t hq, int32_t head_dim, float* out, float* lse,
+                     void* stream) {
+  if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (idx->hkv <= 0 || hq <= 0 || hq % idx->hkv != 0) return SA_ERR_HEAD_COUNT;
+  if (head_dim <= 0) return SA_ERR_BLOCK_PAGE;
+  if (head_dim % 4 != 0 || head_dim > 256) return SA_ERR_UNSUPPORTED;
+  if (!o_partial || !m_partial || !l_partial || !out) return SA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(o_partial) || !aligned16(out)) return SA_ERR_INVALID_ARGUMENT;
+  sa::CombineArgs a{};
+  a.inv = idx->inv;
+  a.edge_head_base = idx->edge_head_base;
+  a.o_partial = o_partial;
+  a.m_partial = m_partial;
+  a.l_partial = l_partial;
+  a.tq = idx->tq;
+  a.hkv = idx->hkv;
+  a.topk = idx->topk;
+  a.qhead = hq / idx->hkv;
+  a.head_dim = head_dim;
+  a.out = out;
+  a.lse = lse;
+  const cudaError_t err = sa::launch_combine(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
+                       int64_t num_pages, sa_dtype kv_dtype, const int32_t* selected, int64_t tq,
+                       int32_t topk, const int64_t* cu_seqlens_q_host,
+                       const int64_t* cu_seqlens_q, int32_t batch, const int32_t* used_kv_lens,
+                       const int32_t* block_tables, int32_t max_pages, int32_t hq, int32_t hkv,
+                       int32_t head_dim, int32_t block_size, int32_t page_size,
+                       float softmax_scale, int32_t causal, int32_t split_edges, sa_index* idx,
+                       float* o_partial, float* m_partial, float* l_partial, float* out,
+                       float* lse, sa_path path, void* stream) {
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
+  if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
+    return SA_ERR_BLOCK_PAGE;
+  if (!sa::forward_cc_supported(head_dim, block_size, kv_dtype == SA_DTYPE_BF16))
+    return SA_ERR_UNSUPPORTED;
+  sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q, batch,
+                                used_kv_lens, max_pages, block_size, page_size, split_edges, idx,
+                                stream);
+  if (st != SA_OK) return st;
+  st = sa_forward(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables, cu_seqlens_q,
+                  used_kv_lens, hq, hkv, head_dim, block_size, page_size, softmax_scale, causal,
+                  o_partial, m_partial, l_partial, path, stream);
+  if (st != SA_OK) return st;
+  return sa_combine(idx, o_partial, m_partial, l_partial, hq, head_dim, out, lse, stream);
+}
+
+sa_status sa_get_status(const sa_index* idx, void* stream) {
+  if (idx == nullptr || idx->totals == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SA_ERR_CUDA;
+  int64_t code = 0;
+  if (cudaMemcpy(&code, idx->totals + 3, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SA_ERR_CUDA;
+  return static_cast<sa_status>(code);
+}
+
+sa_status sa_clear_status(const sa_index* idx, void* stream) {
+  if (idx == nullptr || idx->totals == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  return cudaMemsetAsync(idx->totals + 3, 0, sizeof(int64_t), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,248 @@
+/*
+ * sa.h - C ABI of the KV-outer block-sparse attention library (libsa.so).
+ *
+ * The method (crate alice-llm 2.0.0, module sparse_attention) has three steps:
+ *   1. sa_build_index: invert the per-query top-K block selection into a CSR
+ *      index keyed by (kv head, sparse block)       - types.rs, KvOuterIndex
+ *   2. sa_forward:     for each (kv head, block) work unit, load the block's
+ *      pages once and emit unnormalised softmax partials (o, m, l) for every
+ *      (query, rank) edge and GQA lane pointing at it  - forward.rs,
+ *      kvouter_forward / process_work_unit
+ *   3. sa_combine:     merge each (query, q-head)'s partials with the
+ *      log-sum-exp rule                              - forward.rs, module doc
+ * sa_attention runs the three in sequence on one stream with no host sync.
+ *
+ * Conventions for every entry point:
+ *   - Array arguments are DEVICE pointers unless the name ends in _host.  The
+ *     caller owns and allocates every buffer; the library allocates nothing.
+ *   - Layouts are row-major and contiguous; shapes are given in brackets.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; they return after host-side checks.
+ *   - Host-side checks (shapes, geometry, alignment) return an error status
+ *     and enqueue nothing.  Errors that depend on device data (a selected id
+ *     outside [-1, msb), a page id >= num_pages) are written to the device
+ *     status word of the index (sa_index.totals[3]); outputs are then
+ *     unspecified but every access stays in bounds.  sa_get_status reads it.
+ *   - No kernel traps or waits without a bound: a wait that runs out sets
+ *     SA_ERR_DEVICE_TIMEOUT in the status word and the kernel returns.
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Error kinds.  1..7 follow SparseAttentionError (types.rs) in order;
+ * GpuInitFailed / GpuRuntimeError become SA_ERR_CUDA. */
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_HEAD_COUNT = 1,       /* hq, hkv >= 1 and hq % hkv == 0 required           */
+  SA_ERR_BLOCK_PAGE = 2,       /* head_dim, block_size, page_size > 0 and
+                                  block_size % page_size == 0 required             */
+  SA_ERR_CU_SEQLENS = 3,       /* cu_seqlens_q: >= 2 entries, [0] == 0, non-decreasing */
+  SA_ERR_SHAPE = 4,            /* a size disagrees (cu_seqlens_q[B] != tq, index vs
+                                  call geometry), or a page id >= num_pages (device) */
+  SA_ERR_SELECTED_RANGE = 5,   /* a selected id outside [-1, msb) (device)          */
+  SA_ERR_HEAD_DIM = 6,         /* reserved: q / cache head dims disagree            */
+  SA_ERR_EMPTY = 7,            /* tq == 0, hkv == 0 or topk == 0                    */
+  SA_ERR_CUDA = 8,             /* a CUDA runtime call failed                        */
+  SA_ERR_DEVICE_TIMEOUT = 9,   /* a bounded device wait ran out                     */
+  SA_ERR_UNSUPPORTED = 10,     /* valid for the method, outside what the kernels
+                                  implement (see sa_forward)                       */
+  SA_ERR_INVALID_ARGUMENT = 11 /* NULL or misaligned pointer, too-small workspace   */
+} sa_status;
+
+typedef enum sa_dtype {
+  SA_DTYPE_F32 = 0,
+  SA_DTYPE_BF16 = 1
+} sa_dtype;
+
+/* Forward kernel choice (sa_forward / sa_attention `path`). */
+typedef enum sa_path {
+  SA_PATH_AUTO = 0,          /* pick per problem shape                          */
+  SA_PATH_CUDA_CORE = 1,     /* f32 FMA kernel, any supported shape             */
+  SA_PATH_TENSOR_CORE = 2    /* tcgen05 kernel; SA_ERR_UNSUPPORTED where absent */
+} sa_path;
+
+/*
+ * The KV-outer index (KvOuterIndex, types.rs) plus the work list of the
+ * forward (WorkSplit, scheduler).  Geometry fields are written by
+ * sa_build_index; the caller fills the array pointers (sizes from
+ * sa_index_query_sizes) before the call and must keep them alive and
+ * unmodified until the forward and combine that use the index have run.
+ *
+ *   msb  = floor(max_pages / pages_per_block) blocks per block-table row
+ *   nbs  = batch * msb raw slots per kv head; raw slot = b * msb + block
+ *   E    = number of kept (query, rank) edges          (totals[0])
+ */
+typedef struct sa_index {
+  /* geometry (written by sa_build_index) */
+  int64_t tq;
+  int32_t hkv;
+  int32_t topk;
+  int32_t batch;
+  int32_t max_pages;
+  int32_t block_size;
+  int32_t page_size;
+  int32_t pages_per_block;
+  int32_t msb;
+  int64_t nbs;
+  int32_t split_edges;       /* largest number of edges in one work split (0 = no cut) */
+  int32_t reserved_;
+
+  /* device arrays, caller-allocated */
+  int32_t *sel_slots;        /* [hkv, nbs]   compact slot j -> raw slot; -1 for j >= num_sel[h] */
+  int32_t *sel_offsets;      /* [hkv, nbs+1] head-local CSR offsets; equal to the head's
+                                edge total for j >= num_sel[h] (plateau)                       */
+  int32_t *num_sel;          /* [hkv]        non-empty compact slots per head                  */
+  int64_t *edge_head_base;   /* [hkv+1]      head h owns edges [base[h], base[h+1])            */
+  int32_t *edges;            /* [tq*hkv*topk, 2] (query, rank) pairs in CSR order; first E valid */
+  int32_t *inv;              /* [hkv, tq, topk] head-local edge position, -1 = dropped          */
+  int32_t *splits;           /* [tq*hkv*topk, 4] work list (head, compact slot, abs edge start,
+                                abs edge end) in CSR order; first totals[1] valid               */
+  int64_t *totals;           /* [4] E, number of splits, number of non-empty (head, slot) units,
+                                device status (an sa_status, 0 = none)                         */
+  void *workspace;           /* scratch, sa_index_sizes.workspace_bytes, 256-byte aligned       */
+  size_t workspace_bytes;
+} sa_index;
+
+/* Element counts of each sa_index array and the workspace size in bytes. */
+typedef struct sa_index_sizes {
+  int64_t msb;
+  int64_t nbs;
+  int64_t sel_slots;         /* int32 elements */
+  int64_t sel_offsets;       /* int32 elements */
+  int64_t num_sel;           /* int32 elements */
+  int64_t edge_head_base;    /* int64 elements */
+  int64_t edges;             /* int32 elements (2 per edge)  */
+  int64_t inv;               /* int32 elements */
+  int64_t splits;            /* int32 elements (4 per split) */
+  int64_t totals;            /* int64 elements */
+  size_t workspace_bytes;
+} sa_index_sizes;
+
+/* Human-readable text of a status (the Display strings of
+ * SparseAttentionError, types.rs, where one exists).  Never NULL. */
+const char *sa_status_string(sa_status status);
+
+/* Library version string. */
+const char *sa_version(void);
+
+/*
+ * Sizes for an index over selected[tq, hkv, topk] with `batch` sequences and
+ * block tables of `max_pages` columns.  Fails with SA_ERR_BLOCK_PAGE,
+ * SA_ERR_EMPTY, SA_ERR_UNSUPPORTED (msb above 24576, or tq*hkv*topk >= 2^31)
+ * or SA_ERR_INVALID_ARGUMENT (out == NULL).
+ */
+sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t batch,
+                               int32_t max_pages, int32_t block_size, int32_t page_size,
+                               sa_index_sizes *out);
+
+/*
+ * Step 1: build the KV-outer CSR index (build_kvouter_index; fields of
+ * KvOuterIndex in types.rs).
+ *
+ *   selected          [tq, hkv, topk] int32, -1 = padding (SparseSelection)
+ *   cu_seqlens_q_host [batch+1] int64 on the HOST (validated here, no sync)
+ *   cu_seqlens_q      [batch+1] int64 on the device, same values
+ *   used_kv_lens      [batch] int32 or NULL (NULL: every sequence spans
+ *                     msb * block_size keys)
+ *   max_pages         columns of the block tables; msb = max_pages / (block_size / page_size)
+ *   split_edges       cut each (head, slot) unit's edge range into work splits of
+ *                     at most this many edges (0 = one split per unit)
+ *
+ * An entry (query i, head h, rank r) with block s is kept iff s >= 0 and
+ * s * block_size < max(used_kv_lens[b], 0), b the sequence of i.  Compact
+ * slots are in ascending raw-slot order and each slot's edges in ascending
+ * (query, rank) order.  Checks, in order: BLOCK_PAGE, EMPTY, CU_SEQLENS,
+ * SHAPE (cu_seqlens_q_host[batch] != tq), UNSUPPORTED, INVALID_ARGUMENT;
+ * on device: SELECTED_RANGE.  Enqueues a memset and two kernels on `stream`.
+ */
+sa_status sa_build_index(const int32_t *selected, int64_t tq, int32_t hkv, int32_t topk,
+                         const int64_t *cu_seqlens_q_host, const int64_t *cu_seqlens_q,
+                         int32_t batch, const int32_t *used_kv_lens, int32_t max_pages,
+                         int32_t block_size, int32_t page_size, int32_t split_edges,
+                         sa_index *idx, void *stream);
+
+/*
+ * Step 2: per-edge partials (kvouter_forward, forward.rs).
+ *
+ *   q             [tq, hq, head_dim] float32, 16-byte aligned
+ *   k_pages,
+ *   v_pages       [num_pages, hkv, page_size, head_dim] of kv_dtype, 16-byte aligned
+ *   idx           an index built by sa_build_index on the same stream
+ *   block_tables  [batch, max_pages] int32 physical page per logical page;
+ *                 -1 = no page (its keys are skipped); only pages overlapping a
+ *                 kept block's live range are read
+ *   cu_seqlens_q, used_kv_lens  as for sa_build_index (device)
+ *   softmax_scale scores are softmax_scale * <q, k>
+ *   causal        nonzero: key at absolute position p is live for query i of
+ *                 sequence b iff p <= lk_b - qo_b + (i - cu[b]) when
+ *                 lk_b >= qo_b, else p <= i - cu[b] (right-aligned)
+ *   o_partial     [tq*hkv*topk*qhead, head_dim] float32; rows e*qhead + qh
+ *   m_partial,
+ *   l_partial     [tq*hkv*topk*qhead] float32
+ *
+ * Row e*qhead+qh of the partials (e an edge in CSR order, qh the GQA lane,
+ * q-head h*qhead+qh) holds m = max_p s_p, l = sum_p exp(s_p - m),
+ * o = sum_p exp(s_p - m) v_p over the live keys of its block; a row with no
+ * live key holds (o = 0, m = -inf, l = 0).  Only the first E*qhead rows are
+ * written.  Supported: head_dim a multiple of 4 (f32) or 8 (bf16), at most
+ * 256, and block_size * head_dim * elt * 2 <= 160 KiB; otherwise
+ * SA_ERR_UNSUPPORTED.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
+ */
+sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
+                     int64_t num_pages, sa_dtype kv_dtype, const sa_index *idx,
+                     const int32_t *block_tables, const int64_t *cu_seqlens_q,
+                     const int32_t *used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
+                     int32_t block_size, int32_t page_size, float softmax_scale, int32_t causal,
+                     float *o_partial, float *m_partial, float *l_partial, sa_path path,
+                     void *stream);
+
+/*
+ * Step 3: log-sum-exp combine (forward.rs module doc: "standard FlashAttention
+ * log-sum-exp update").  For query i and q-head hq (h = hq / qhead), over
+ * ranks r with inv[h, i, r] >= 0: M = max m_r, L = sum exp(m_r - M) l_r,
+ * out[i, hq] = sum exp(m_r - M) o_r / L, lse[i, hq] = M + log L.  A row with
+ * no live partial gets out = 0 and lse = -inf.
+ *
+ *   out  [tq, hq, head_dim] float32 (16-byte aligned)
+ *   lse  [tq, hq] float32 or NULL
+ */
+sa_status sa_combine(const sa_index *idx, const float *o_partial, const float *m_partial,
+                     const float *l_partial, int32_t hq, int32_t head_dim, float *out,
+                     float *lse, void *stream);
+
+/*
+ * Steps 1-3 on one stream, no host synchronisation (kvouter_attention, the
+ * fused public entry of the module).  Arguments as above; `idx` carries the
+ * caller's index arrays and workspace and is filled in as by sa_build_index.
+ * The partial buffers are scratch of the sizes sa_forward documents.
+ */
+sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,
+                       int64_t num_pages, sa_dtype kv_dtype, const int32_t *selected,
+                       int64_t tq, int32_t topk, const int64_t *cu_seqlens_q_host,
+                       const int64_t *cu_seqlens_q, int32_t batch, const int32_t *used_kv_lens,
+                       const int32_t *block_tables, int32_t max_pages, int32_t hq, int32_t hkv,
+                       int32_t head_dim, int32_t block_size, int32_t page_size,
+                       float softmax_scale, int32_t causal, int32_t split_edges, sa_index *idx,
+                       float *o_partial, float *m_partial, float *l_partial, float *out,
+                       float *lse, sa_path path, void *stream);
+
+/* Synchronises `stream` and returns the first device-detected error recorded
+ * in idx->totals[3] (SA_OK if none), or SA_ERR_CUDA if the stream failed. */
+sa_status sa_get_status(const sa_index *idx, void *stream);
+
+/* Clears the device status word of an index (enqueued on `stream`). */
+sa_status sa_clear_status(const sa_index *idx, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

@@ -1,0 +1,122 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and its host-side checks return the documented status codes before
+any device work is enqueued."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_paged_csr_gb300 import _native
+
+    if not os.path.exists(_native.LIB_PATH):
+        from block_sparse_paged_csr_gb300 import build
+
+        build.build_library()
+    return _native.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    from block_sparse_paged_csr_gb300 import _native
+
+    assert header_functions() == sorted(_native.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    for name in header_functions():
+        assert re.search(rf"\bT {name}\b", out), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    from block_sparse_paged_csr_gb300 import _native
+
+    for code in _native.STATUS_NAMES:
+        assert lib.sa_status_string(code)
+    assert b"multiple of Hkv" in lib.sa_status_string(1)
+    assert b"sm_103a" in lib.sa_version()
+
+
+def test_index_sizes_of_the_serving_workloads(lib):
+    from block_sparse_paged_csr_gb300 import _native
+
+    s = _native.SaIndexSizes()
+    # GQA decode: B=64, 1 query each, Hkv=8, topk=16, max_pages=2048, page 16, block 64
+    assert lib.sa_index_query_sizes(64, 8, 16, 64, 2048, 64, 16, ctypes.byref(s)) == 0
+    assert (s.msb, s.nbs) == (512, 32768)
+    assert s.sel_offsets == 8 * 32769 and s.inv == 64 * 8 * 16 and s.edges == 2 * 8192
+    # long-context decode: B=128, Hkv=8, topk=64, max_pages=8192
+    assert lib.sa_index_query_sizes(128, 8, 64, 128, 8192, 64, 16, ctypes.byref(s)) == 0
+    assert (s.msb, s.nbs) == (2048, 262144)
+
+
+def _build(lib, **kw):
+    from block_sparse_paged_csr_gb300 import _native
+
+    a = dict(selected=None, tq=4, hkv=2, topk=2, cu=np.array([0, 4], np.int64), cu_dev=None,
+             batch=1, used=None, max_pages=16, bs=32, ps=16, split=0)
+    a.update(kw)
+    idx = _native.SaIndex()
+    cu = a["cu"]
+    return lib.sa_build_index(a["selected"], a["tq"], a["hkv"], a["topk"],
+                              cu.ctypes.data_as(ctypes.c_void_p) if cu is not None else None,
+                              a["cu_dev"], a["batch"], a["used"], a["max_pages"], a["bs"],
+                              a["ps"], a["split"], ctypes.byref(idx), None)
+
+
+def test_build_index_host_checks(lib):
+    names = {v: k for k, v in __import__("block_sparse_paged_csr_gb300._native",
+                                         fromlist=["x"]).STATUS_NAMES.items()}
+    assert _build(lib, bs=24, ps=16) == names["BLOCK_PAGE"]
+    assert _build(lib, bs=0) == names["BLOCK_PAGE"]
+    assert _build(lib, tq=0) == names["EMPTY"]
+    assert _build(lib, topk=0) == names["EMPTY"]
+    assert _build(lib, hkv=0) == names["EMPTY"]
+    assert _build(lib, cu=np.array([1, 4], np.int64)) == names["CU_SEQLENS"]
+    assert _build(lib, cu=np.array([0, 3, 2, 4], np.int64), batch=3) == names["CU_SEQLENS"]
+    assert _build(lib, cu=np.array([0, 3], np.int64)) == names["SHAPE"]
+    assert _build(lib, max_pages=2 * 24577) == names["UNSUPPORTED"]
+    # everything valid but no device arrays: rejected before any launch
+    assert _build(lib) == names["INVALID_ARGUMENT"]
+
+
+def test_forward_and_combine_host_checks(lib):
+    from block_sparse_paged_csr_gb300 import _native
+
+    names = {v: k for k, v in _native.STATUS_NAMES.items()}
+    idx = _native.SaIndex(hkv=2, pages_per_block=2, block_size=32, page_size=16, tq=4, topk=2)
+
+    def fwd(hq=4, hkv=2, d=32, bs=32, ps=16, dtype=0, path=0, ptrs=False):
+        p = ctypes.c_void_p(16) if ptrs else None
+        return lib.sa_forward(p, p, p, 16, dtype, ctypes.byref(idx), p, p, None, hq, hkv, d, bs,
+                              ps, 0.1, 0, p, p, p, path, None)
+
+    assert fwd(hq=3) == names["HEAD_COUNT"]
+    assert fwd(hkv=0) == names["HEAD_COUNT"]
+    assert fwd(bs=24) == names["BLOCK_PAGE"]
+    assert fwd(d=0) == names["BLOCK_PAGE"]
+    assert fwd(bs=64) == names["SHAPE"]          # index built for another block size
+    assert fwd(d=30) == names["UNSUPPORTED"]
+    assert fwd(d=512) == names["UNSUPPORTED"]
+    assert fwd(dtype=1, d=36) == names["UNSUPPORTED"]
+    assert fwd(dtype=7) == names["INVALID_ARGUMENT"]
+    assert fwd() == names["INVALID_ARGUMENT"]      # null pointers
+    assert lib.sa_combine(ctypes.byref(idx), None, None, None, 3, 32, None, None, None) == \
+        names["HEAD_COUNT"]
+    assert lib.sa_combine(ctypes.byref(idx), None, None, None, 4, 30, None, None, None) == \
+        names["UNSUPPORTED"]

@@ -1,0 +1,191 @@
+"""Parity of the CUDA library (through its C ABI) with the oracle.
+
+* Index: bit-exact, every array, on every workload shape and random edge cases.
+* Partials and outputs: element by element within the f32 tolerance (1e-4,
+  row-normalised) on reduced workloads the oracle finishes in seconds.
+* Full-size serving workloads (the launch configuration the benchmark times):
+  the index bit-exact, outputs on sampled (query, q-head) rows recomputed by
+  the oracle's query-outer attention.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import _pins
+import block_sparse_paged_csr_gb300 as sa
+import inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "gqa_decode", "chunked_prefill", "chunked_prefill_bf16", "skewed",
+         "long_decode"]
+
+
+def _oracle_attention(w, split_edges):
+    return oracle.attention(w.q_host(), w.k_host(), w.v_host(), w.selected, w.block_tables,
+                            w.cu_seqlens_q, w.used, w.hq, w.head_dim, w.block_size, w.page_size,
+                            w.softmax_scale, w.causal, split_edges=split_edges)
+
+
+@pytest.mark.parametrize("split", [0, 3])
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workload_parity(name, split):
+    w = inputs.small(name, seed=0)
+    t = _gpu.device_workload(w)
+    out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=split)
+    ref_out, ref_lse, ref_idx, (ro, rm, rl) = _oracle_attention(w, split)
+    _gpu.compare_index(idx.to_host(), ref_idx)
+    rows = ref_idx["edges"].shape[0] * w.qhead
+    _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(), l[:rows].cpu().numpy(),
+                          ro, rm, rl, _gpu.TOL_F32)
+    assert _gpu.row_error(out.cpu().numpy(), ref_out) <= _gpu.TOL_F32
+    _gpu.compare_lse(lse.cpu().numpy(), ref_lse, _gpu.TOL_F32)
+
+
+def _case_tensors(c, dev="cuda"):
+    k, v = c["k"], c["v"]
+    if k.dtype == np.uint16:
+        kt = torch.from_numpy(k.view(np.int16)).to(dev).view(torch.bfloat16)
+        vt = torch.from_numpy(v.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        kt, vt = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+    return dict(q=torch.from_numpy(c["q"]).to(dev), k=kt, v=vt,
+                selected=torch.from_numpy(c["sel"]).to(dev),
+                cu=torch.from_numpy(c["cu"]).to(dev),
+                used=None if c["used"] is None else torch.from_numpy(c["used"]).to(dev),
+                bt=torch.from_numpy(c["bt"]).to(dev))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_edge_cases(seed):
+    """Empty sequences, page holes (-1), blocks past the KV length, repeated
+    blocks, used_kv_lens = None, GQA, several pages per block, both masks."""
+    bf16 = seed % 3 == 0
+    c = _pins.random_case(seed, bf16=bf16, full=bool(seed % 2))
+    if bf16 and c["d"] % 8:
+        c = _pins.random_case(seed + 100, bf16=True, full=bool(seed % 2))
+        if c["d"] % 8:
+            pytest.skip("bf16 needs head_dim % 8 == 0")
+    if seed % 5 == 0 and c["sel"].shape[2] > 1:
+        c["sel"][..., 1] = c["sel"][..., 0]
+    t = _case_tensors(c)
+    for causal in (False, True):
+        split = seed % 3
+        out, lse, idx, (o, m, l) = sa.sa_attention(
+            t["q"], t["k"], t["v"], t["selected"], c["cu"], t["cu"], t["used"], t["bt"], c["hq"],
+            c["hkv"], c["d"], c["bs"], c["ps"], c["scale"], causal, split_edges=split)
+        assert sa.sa_get_status(idx) == 0
+        ref_out, ref_lse, ref_idx, (ro, rm, rl) = oracle.attention(
+            c["q"], c["k"], c["v"], c["sel"], c["bt"], c["cu"], c["used"], c["hq"], c["d"],
+            c["bs"], c["ps"], c["scale"], causal, split_edges=split)
+        _gpu.compare_index(idx.to_host(), ref_idx)
+        rows = ref_idx["edges"].shape[0] * (c["hq"] // c["hkv"])
+        _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(),
+                              l[:rows].cpu().numpy(), ro, rm, rl, _gpu.TOL_F32)
+        assert _gpu.row_error(out.cpu().numpy(), ref_out) <= _gpu.TOL_F32
+        _gpu.compare_lse(lse.cpu().numpy(), ref_lse, _gpu.TOL_F32)
+
+
+def test_separate_steps_match_fused():
+    w = inputs.small("skewed", seed=2)
+    t = _gpu.device_workload(w)
+    out_f, lse_f, _, _ = _gpu.run_attention(w, t, split_edges=4)
+    idx = sa.sa_build_index(t["selected"], w.cu_seqlens_q, t["cu"], t["used"], w.max_pages,
+                            w.block_size, w.page_size, split_edges=4)
+    o, m, l = sa.sa_forward(t["q"], t["k"], t["v"], idx, t["bt"], t["cu"], t["used"], w.hq, w.hkv,
+                            w.head_dim, w.block_size, w.page_size, w.softmax_scale, w.causal)
+    out, lse = sa.sa_combine(idx, o, m, l, w.hq, w.head_dim)
+    assert sa.sa_get_status(idx) == 0
+    assert torch.equal(out, out_f) and torch.equal(lse, lse_f)
+
+
+def test_all_padding_gives_zero_output():
+    w = inputs.small("gqa_decode", seed=3)
+    w.selected[:] = -1
+    t = _gpu.device_workload(w)
+    out, lse, idx, _ = _gpu.run_attention(w, t)
+    assert int(idx.totals[0]) == 0
+    assert torch.count_nonzero(out) == 0
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_device_detected_errors_are_reported():
+    w = inputs.small("tiny", seed=0)
+    t = _gpu.device_workload(w)
+    bad = t["selected"].clone()
+    bad[1, 0, 1] = w.msb                                   # outside [-1, msb)
+    _, _, idx, _ = sa.sa_attention(t["q"], t["k"], t["v"], bad, w.cu_seqlens_q, t["cu"],
+                                   t["used"], t["bt"], w.hq, w.hkv, w.head_dim, w.block_size,
+                                   w.page_size, w.softmax_scale, w.causal)
+    assert sa.sa_get_status(idx) == 5                      # SELECTED_RANGE
+    bt = t["bt"].clone()
+    blk = int(w.selected[0, 0, 0])
+    bt[0, blk * w.ppb] = w.num_pages                       # page id == num_pages
+    _, _, idx, _ = sa.sa_attention(t["q"], t["k"], t["v"], t["selected"], w.cu_seqlens_q, t["cu"],
+                                   t["used"], bt, w.hq, w.hkv, w.head_dim, w.block_size,
+                                   w.page_size, w.softmax_scale, w.causal)
+    assert sa.sa_get_status(idx) == 4                      # SHAPE
+    # a clean call afterwards reports nothing
+    _, _, idx, _ = _gpu.run_attention(w, t)
+
+
+def test_host_checks_raise():
+    w = inputs.small("tiny", seed=0)
+    t = _gpu.device_workload(w)
+    with pytest.raises(sa.SAError, match="HEAD_COUNT"):
+        sa.sa_attention(t["q"], t["k"], t["v"], t["selected"], w.cu_seqlens_q, t["cu"], t["used"],
+                        t["bt"], 3, w.hkv, w.head_dim, w.block_size, w.page_size, 0.1, False)
+    with pytest.raises(sa.SAError, match="SHAPE"):
+        bad_cu = w.cu_seqlens_q.copy()
+        bad_cu[-1] += 1
+        sa.sa_build_index(t["selected"], bad_cu, t["cu"], t["used"], w.max_pages, w.block_size,
+                          w.page_size)
+
+
+def test_device_fill_matches_host_generator():
+    for dtype in ("f32", "bf16"):
+        n = 1 << 20
+        dev = torch.empty(n, dtype=torch.float32 if dtype == "f32" else torch.bfloat16,
+                          device="cuda")
+        inputs.fill_device(dev, 7, inputs.STREAM_V, start=12345, bf16=dtype == "bf16")
+        host = inputs.counter_normal(7, inputs.STREAM_V, 12345, n)
+        if dtype == "bf16":
+            got = dev.view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, inputs.bf16_bits(host))
+        else:
+            assert np.array_equal(dev.cpu().numpy(), host)
+
+
+# --------------------------------------------------------------------------- full size
+
+FULL = ["gqa_decode", "chunked_prefill", "chunked_prefill_bf16", "skewed", "long_decode"]
+SPLIT = {"gqa_decode": 0, "chunked_prefill": 16, "chunked_prefill_bf16": 16, "skewed": 16,
+         "long_decode": 0}
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    """The serving workloads at full size: index bit-exact against the oracle,
+    outputs on sampled rows against the oracle's query-outer attention."""
+    w = inputs.FULL[name](0)
+    t = _gpu.device_workload(w, fill_on_device=True)
+    out, lse, idx, _ = _gpu.run_attention(w, t, split_edges=SPLIT[name])
+    ref_idx = oracle.build_index(w.selected, w.cu_seqlens_q, w.used, w.max_pages, w.block_size,
+                                 w.page_size, SPLIT[name])
+    _gpu.compare_index(idx.to_host(), ref_idx)
+    rng = np.random.default_rng(11)
+    n_q = 6 if name == "long_decode" else 12
+    queries = np.unique(rng.choice(w.tq, size=n_q, replace=False))
+    k, v, bt, num_pages = w.compact_pool(queries)
+    rows = np.array([(i, hq) for i in queries for hq in rng.choice(w.hq, 4, replace=False)])
+    q = w.q_host()
+    ref, ref_lse = oracle.direct(q, k, v, w.selected, bt, w.cu_seqlens_q, w.used, w.hq,
+                                 w.head_dim, w.block_size, w.page_size, w.softmax_scale,
+                                 w.causal, rows=rows)
+    got = out[rows[:, 0], rows[:, 1]].cpu().numpy()
+    assert _gpu.row_error(got, ref) <= _gpu.TOL_F32
+    _gpu.compare_lse(lse[rows[:, 0], rows[:, 1]].cpu().numpy(), ref_lse, _gpu.TOL_F32)
+    del t
+    torch.cuda.empty_cache()
