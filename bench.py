@@ -1,0 +1,517 @@
+"""Benchmark of KV-outer block-sparse paged attention (index + forward +
+combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+One step is one pass of the whole path (sa_attention: CSR index build,
+KV-outer forward, log-sum-exp combine) over one batch of the workload, with
+every input resident in HBM.  Between timed steps L2 is flushed by writing a
+512 MiB buffer (outside the step's CUDA events).  Prints one JSON line.
+
+--impl reference times the oracle (plain f64 C, one host thread) on a bounded
+sample of the same workload; it is a reported CPU baseline.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (its own
+seed) on its own GPU: the path has no exchange step, so there is no data
+collective; a barrier and a max-reduction of the elapsed time bracket the run.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn fwd queries/s + selected-KV GB/s (% of GB300 HBM roofline)"
+UNIT = "queries/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+SPLIT_EDGES = {"tiny": 0, "gqa_decode": 0, "chunked_prefill": 16, "chunked_prefill_bf16": 16,
+               "skewed": 16, "long_decode": 0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gqa_decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def make_workload(name: str, seed: int):
+    """The five serving workloads, plus reduced-pool variants used only for
+    ncu captures (same per-unit work, pool of a few GB)."""
+    import inputs
+
+    if name == "gqa_decode_ncu":
+        w = inputs.gqa_decode(seed, kv_min=4096, kv_max=6144)
+        w.name = name
+        return w
+    if name == "long_decode_ncu":
+        w = inputs.long_decode(seed, batch=128, kv_min=8192, kv_max=12288)
+        w.name = name
+        return w
+    return inputs.FULL[name](seed)
+
+
+# --------------------------------------------------------------------------- accounting
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes the KV-outer method must move, from the workload's own index
+    inputs: each kept (kv head, block) loads its live keys' K and V once, Q is
+    read once, the partials are written by the forward and read by the
+    combine, the output is written once."""
+    elt = 2 if w.kv_dtype == "bf16" else 4
+    cu = w.cu_seqlens_q
+    kv_keys = 0
+    flops = 0
+    edges = 0
+    for b in range(w.batch):
+        q0, q1 = int(cu[b]), int(cu[b + 1])
+        if q1 == q0:
+            continue
+        lk = max(int(w.used_kv_lens[b]), 0) if w.pass_used else w.msb * w.block_size
+        sel = w.selected[q0:q1]                                   # [qo, hkv, topk]
+        kept = (sel >= 0) & (sel.astype(np.int64) * w.block_size < lk)
+        edges += int(kept.sum())
+        live_pages = (w.block_tables[b] >= 0)
+        for h in range(w.hkv):
+            blocks = np.unique(sel[:, h][kept[:, h]])
+            for blk in blocks:
+                s0 = int(blk) * w.block_size
+                s1 = min(s0 + w.block_size, lk)
+                pos = np.arange(s0, s1)
+                nk = int(np.sum(live_pages[pos // w.page_size]))
+                kv_keys += nk
+                n_e = int(np.sum(sel[:, h][kept[:, h]] == blk))
+                flops += 4 * w.head_dim * nk * n_e * w.qhead        # upper bound (no causal cut)
+    kv = 2 * kv_keys * w.head_dim * elt
+    q = w.tq * w.hq * w.head_dim * 4
+    parts = edges * w.qhead * (w.head_dim + 2) * 4
+    out = w.tq * w.hq * w.head_dim * 4
+    inv = w.hkv * w.tq * w.topk * 4
+    return {"kv": kv, "q": q, "partials_write": parts, "partials_read": parts, "out": out,
+            "inv": inv, "edges": edges, "flops": flops,
+            "forward": kv + q + parts, "combine": parts + inv + out,
+            "step": kv + q + 2 * parts + out}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    src = os.path.join(ROOT, "block_sparse_paged_csr_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", f"{kernel_file.split('.')[0]}_{workload}.md")
+    if not (os.path.exists(src) and os.path.exists(prof)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(prof).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256 ([0-9a-f]+)\)",
+                  text)
+    if not m or m.group(2) != digest:
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        deadline = time.time() + 5
+        while not self.lines and time.time() < deadline:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 - 0.06 <= t <= self.t1 + 0.06] or \
+            [l for (_, l) in self.lines[-3:]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- ours
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import block_sparse_paged_csr_gb300 as sa
+    import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = make_workload(args.workload, args.seed + rank)
+    split = SPLIT_EDGES.get(args.workload.replace("_ncu", ""), 0)
+    acct = algorithmic_bytes(w)
+
+    q, k, v = inputs.device_tensors(w, dev)
+    sel = torch.from_numpy(w.selected).to(dev)
+    cu = torch.from_numpy(w.cu_seqlens_q).to(dev)
+    used = torch.from_numpy(w.used_kv_lens).to(dev) if w.pass_used else None
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cu_host = w.cu_seqlens_q
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(index=None, partials=None, out=None, lse=None):
+        return sa.sa_attention(q, k, v, sel, cu_host, cu, used, bt, w.hq, w.hkv, w.head_dim,
+                               w.block_size, w.page_size, w.softmax_scale, w.causal,
+                               split_edges=split, index=index, partials=partials, out=out,
+                               lse=lse)
+
+    out, lse, index, partials = step()
+    torch.cuda.synchronize(dev)
+    status = sa.sa_get_status(index)
+    if status != 0:
+        raise RuntimeError(f"device status {sa.sa_status_string(status)}")
+    for _ in range(max(args.warmup, 3)):
+        step(index, partials, out, lse)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps of the fused path ----------------------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier()
+    clocks.mark(True)
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        starts[s].record(stream)
+        step(index, partials, out, lse)
+        ends[s].record(stream)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clocks.mark(False)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    status = sa.sa_get_status(index)
+    if status != 0:
+        raise RuntimeError(f"device status {sa.sa_status_string(status)}")
+
+    # ---- per-stage durations (same launches, events between the stages) -----
+    n_stage = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_stage)]
+    o_p, m_p, l_p = partials
+    for s in range(n_stage):
+        flush.fill_(float(s))
+        e = ev[s]
+        e[0].record(stream)
+        sa.sa_build_index(sel, cu_host, cu, used, w.max_pages, w.block_size, w.page_size,
+                          split_edges=split, index=index)
+        e[1].record(stream)
+        sa.sa_forward(q, k, v, index, bt, cu, used, w.hq, w.hkv, w.head_dim, w.block_size,
+                      w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p)
+        e[2].record(stream)
+        sa.sa_combine(index, o_p, m_p, l_p, w.hq, w.head_dim, out, lse)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    st = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])
+    index_ms, fwd_ms, comb_ms = (float(x) for x in st.mean(axis=0))
+
+    # ---- end to end through the public API with host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        h_q = q.cpu().pin_memory()
+        h_sel, h_bt, h_cu = pin(w.selected), pin(w.block_tables), pin(w.cu_seqlens_q)
+        h_used = pin(w.used_kv_lens) if w.pass_used else None
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_sel, h_bt, h_cu, h_used)
+                  if t is not None)
+        d2h = h_out.numel() * 4 + h_lse.numel() * 4
+        d_q, d_sel, d_bt, d_cu = (torch.empty_like(x, device=dev) for x in (h_q, h_sel, h_bt, h_cu))
+        d_used = torch.empty_like(h_used, device=dev) if h_used is not None else None
+        n_e2e = min(args.steps, 300)
+        s0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        s1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        for it in range(n_e2e + 3):
+            timed = it >= 3
+            flush.fill_(float(it))
+            if timed:
+                s0[it - 3].record(stream)
+            d_q.copy_(h_q, non_blocking=True)
+            d_sel.copy_(h_sel, non_blocking=True)
+            d_bt.copy_(h_bt, non_blocking=True)
+            d_cu.copy_(h_cu, non_blocking=True)
+            if d_used is not None:
+                d_used.copy_(h_used, non_blocking=True)
+            sa.sa_attention(d_q, k, v, d_sel, w.cu_seqlens_q, d_cu, d_used, d_bt, w.hq, w.hkv,
+                            w.head_dim, w.block_size, w.page_size, w.softmax_scale, w.causal,
+                            split_edges=split, index=index, partials=partials, out=out,
+                            lse=lse)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            if timed:
+                s1[it - 3].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(a.elapsed_time(b) for a, b in zip(s0, s1))
+        e2e = {"value": w.tq * n_e2e / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": n_e2e}
+
+    # ---- aggregate over ranks -----------------------------------------------
+    elapsed_s = total_ms / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+        if e2e is not None:
+            t = torch.tensor([e2e["value"]], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MIN)
+            e2e["value"] = float(t.item()) * world
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peak()
+    ms_per_step = elapsed_s * 1e3 / args.steps
+    fwd_gbs = acct["forward"] / (fwd_ms / 1e3) / 1e9
+    step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
+    kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
+    traffic = ncu_traffic("forward_cc.cu", args.workload)
+    value = world * w.tq * args.steps / elapsed_s
+    dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": w.batch, "tq": w.tq, "hq": w.hq, "hkv": w.hkv,
+            "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size,
+            "topk": w.topk, "max_pages": w.max_pages, "num_pages": w.num_pages,
+            "kv_dtype": w.kv_dtype, "causal": w.causal, "split_edges": split,
+            "l2": "flushed before every timed step (512 MiB write, outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "selected_kv_gbs": kv_gbs,
+        "step_algorithmic_gbs": step_gbs,
+        "step_frac_of_hbm": step_gbs / peak,
+        "tflops": acct["flops"] / (ms_per_step / 1e3) / 1e12,
+        "stages_ms": {"index": index_ms, "forward": fwd_ms, "combine": comb_ms},
+        "roofline": {"kernel": "forward_cc_kernel (sa_forward)", "bound": "hbm",
+                     "achieved": fwd_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": fwd_gbs / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": acct["forward"],
+                     "traffic": traffic},
+        "algorithmic_bytes": {k_: acct[k_] for k_ in ("kv", "q", "partials_write", "out",
+                                                       "step", "forward", "combine")},
+        "edges": acct["edges"],
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+        "cpu_baseline": (cpu_baseline(w, args)
+                         if world == 1 and not args.no_cpu_baseline else None),
+    }
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+
+def sub_workload(w, seqs):
+    """The same workload restricted to the given sequences (a bounded sample)."""
+    import dataclasses
+
+    seqs = np.asarray(seqs)
+    cu = w.cu_seqlens_q
+    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in seqs]).astype(np.int64)
+    sub = dataclasses.replace(w, batch=len(seqs), qo_lens=w.qo_lens[seqs],
+                              used_kv_lens=w.used_kv_lens[seqs], selected=w.selected[rows],
+                              block_tables=w.block_tables[seqs])
+    q = w.q_host()[rows]
+    return sub, q
+
+
+def time_oracle(w, seqs, repeat_until_s):
+    """Oracle queries/s on the sample: index + partials + combine."""
+    import oracle
+
+    sub, q = sub_workload(w, seqs)
+    k, v, bt, _ = sub.compact_pool()
+    n = 0
+    t_total = 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, sub.selected, bt, sub.cu_seqlens_q, sub.used, sub.hq,
+                         sub.head_dim, sub.block_size, sub.page_size, sub.softmax_scale,
+                         sub.causal)
+        t_total += time.perf_counter() - t0
+        n += 1
+        if t_total >= repeat_until_s:
+            break
+    return sub.tq * n / t_total, n, sub.tq
+
+
+def sample_sequences(w, target_queries):
+    """Leading sequences of the workload holding about target_queries queries."""
+    acc, seqs = 0, []
+    for b in range(w.batch):
+        seqs.append(b)
+        acc += int(w.qo_lens[b])
+        if acc >= target_queries:
+            break
+    return seqs
+
+
+def cpu_baseline(w, args):
+    import oracle
+
+    oracle.build()
+    target = {"gqa_decode": 16, "long_decode": 4, "tiny": 4}.get(args.workload, 64)
+    seqs = sample_sequences(w, target)
+    qps, n, nq = time_oracle(w, seqs, repeat_until_s=10.0)
+    return {"value": qps, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {len(seqs)} sequence(s) ({nq} queries) of the workload, "
+                      f"full index + partials + combine in f64, repeated {n}x (~10 s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import inputs
+    import oracle
+
+    oracle.build()
+    w = make_workload(args.workload, args.seed)
+    target = {"gqa_decode": 1, "long_decode": 1, "tiny": 4}.get(args.workload, 2)
+    seqs = sample_sequences(w, target)
+    sub, q = sub_workload(w, seqs)
+    k, v, bt, _ = sub.compact_pool()
+
+    def one():
+        oracle.attention(q, k, v, sub.selected, bt, sub.cu_seqlens_q, sub.used, sub.hq,
+                         sub.head_dim, sub.block_size, sub.page_size, sub.softmax_scale,
+                         sub.causal)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = sub.tq * args.steps / el
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample_queries_per_step": sub.tq},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"first {len(seqs)} sequence(s) ({sub.tq} queries) "
+                                       f"per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if res is not None and rank == 0:
+        print(json.dumps(res))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
