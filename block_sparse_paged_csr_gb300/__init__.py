@@ -26,7 +26,8 @@ from . import _native
 from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE,
                       STATUS_NAMES)
 
-__all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index", "sa_forward",
+__all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
+           "sa_build_index_no_alloc", "sa_forward",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE"]
 
@@ -189,6 +190,28 @@ def sa_build_index(selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, max_
         _ptr(selected), tq, hkv, topk, cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q),
         batch, _ptr(used_kv_lens), max_pages, block_size, page_size, split_edges,
         ctypes.byref(index.c), _stream(stream, dev)), "sa_build_index")
+    return index
+
+
+def sa_build_index_no_alloc(selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, index: Index,
+                            max_pages, block_size, page_size, split_edges=0, stream=None) -> Index:
+    """Step 1 with the build's scratch taken from a fixed array inside the
+    library instead of ``index.workspace``: for callers that cannot allocate
+    device memory at call time.  ``index`` must already hold the output arrays
+    (see :func:`allocate_index`).  Calls that overlap on the GPU share that
+    array and race; the first call on a device must come before any stream
+    capture on it."""
+    _require(selected, torch.int32, "selected")
+    dev = selected.device
+    tq, hkv, topk = (int(x) for x in selected.shape)
+    cu_h = _host_i64(cu_seqlens_q_host)
+    _require(cu_seqlens_q, torch.int64, "cu_seqlens_q", dev)
+    if used_kv_lens is not None:
+        _require(used_kv_lens, torch.int32, "used_kv_lens", dev)
+    _check(_native.load().sa_build_index_no_alloc(
+        _ptr(selected), tq, hkv, topk, cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q),
+        cu_h.size - 1, _ptr(used_kv_lens), max_pages, block_size, page_size, split_edges,
+        ctypes.byref(index.c), _stream(stream, dev)), "sa_build_index_no_alloc")
     return index
 
 

@@ -19,7 +19,7 @@ PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",
-           "sa_forward", "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status")
+           "sa_build_index_no_alloc", "sa_forward", "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status")
 
 
 class SaIndex(ctypes.Structure):
@@ -79,6 +79,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_build_index.argtypes = [p, i64, i32, i32, p, p, i32, p, i32, i32, i32, i32,
                                    ctypes.POINTER(SaIndex), p]
     lib.sa_build_index.restype = st
+    lib.sa_build_index_no_alloc.argtypes = lib.sa_build_index.argtypes
+    lib.sa_build_index_no_alloc.restype = st
     lib.sa_forward.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, i32, i32, i32,
                                i32, i32, f32, i32, p, p, p, st, p]
     lib.sa_forward.restype = st

@@ -1,0 +1,84 @@
+// sa_build_index_no_alloc: the index build with its scratch memory taken from
+// a fixed array compiled into this library instead of a caller-provided
+// workspace.
+//
+// Who needs it: callers that must not allocate device memory at call time:
+// an inference server whose memory pool is fixed at start-up, code running
+// where a cudaMalloc would synchronise the device or fail under a memory cap,
+// or a host runtime that has no allocator to hand.  They still own the index
+// arrays and the selection inputs; only the scratch moves into the library.
+//
+// The scratch holds the index kernel's segment ticket and per-segment status
+// words (see index.cu).  Every GPU that loads this library keeps its own copy
+// of the array until the process exits.
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "sa.h"
+
+namespace {
+
+// 288 KiB: enough for hkv * batch up to about 18,000 (kv head, sequence)
+// segments.
+constexpr size_t kStaticScratchBytes = 288 * 1024;
+
+static __device__ __align__(256) unsigned char g_index_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_index_scratch on the current device, looked up once per
+// device.  The name g_index_scratch in host code is only a host-side stand-in,
+// so the address must come from cudaGetSymbolAddress with that device current.
+sa_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr)
+      return SA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" sa_status sa_build_index_no_alloc(const int32_t* selected, int64_t tq, int32_t hkv,
+                                             int32_t topk, const int64_t* cu_seqlens_q_host,
+                                             const int64_t* cu_seqlens_q, int32_t batch,
+                                             const int32_t* used_kv_lens, int32_t max_pages,
+                                             int32_t block_size, int32_t page_size,
+                                             int32_t split_edges, sa_index* idx, void* stream) {
+  if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (hkv > 0 && batch > 0 &&
+      sa::workspace_layout(hkv, batch).total > kStaticScratchBytes)
+    return SA_ERR_UNSUPPORTED;  // more (kv head, sequence) segments than the scratch holds
+  void* scratch = nullptr;
+  if (hkv > 0 && batch > 0) {
+    const sa_status st = scratch_for_current_device(&scratch);
+    if (st != SA_OK) return st;
+  }
+  // Run the regular build on a copy of the caller's index whose workspace is
+  // the static scratch; the build clears the part of it that must start at
+  // zero on the stream before its kernels run.
+  sa_index local = *idx;
+  local.workspace = scratch;
+  local.workspace_bytes = kStaticScratchBytes;
+  const sa_status st =
+      sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q, batch,
+                     used_kv_lens, max_pages, block_size, page_size, split_edges, &local, stream);
+  if (st == SA_OK) {
+    void* keep_ws = idx->workspace;
+    const size_t keep_bytes = idx->workspace_bytes;
+    *idx = local;
+    idx->workspace = keep_ws;
+    idx->workspace_bytes = keep_bytes;
+  }
+  return st;
+}

@@ -169,6 +169,35 @@ sa_status sa_build_index(const int32_t *selected, int64_t tq, int32_t hkv, int32
                          sa_index *idx, void *stream);
 
 /*
+ * sa_build_index without a workspace: the pages have no counterpart; this is
+ * a library convenience.  Same arguments, checks and results as
+ * sa_build_index, except that idx->workspace / workspace_bytes are ignored
+ * (left unchanged) and the build's scratch comes from a 288 KiB array
+ * compiled into the library, one copy per GPU that loads it, held until the
+ * process exits.
+ *
+ * For callers that cannot allocate device memory when they call: servers
+ * whose device memory is reserved up front, code running under a memory cap,
+ * or host runtimes without a device allocator.  The call itself allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ *   - Returns SA_ERR_UNSUPPORTED when hkv * batch (kv head, sequence)
+ *     segments need more scratch than the array holds (about 18,000).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one array per device, and each call clears the
+ *     part that must start at zero on its stream.  Calls whose work overlaps
+ *     on the GPU (other streams, other threads) race on it: serialise them.
+ */
+sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t hkv,
+                                  int32_t topk, const int64_t *cu_seqlens_q_host,
+                                  const int64_t *cu_seqlens_q, int32_t batch,
+                                  const int32_t *used_kv_lens, int32_t max_pages,
+                                  int32_t block_size, int32_t page_size, int32_t split_edges,
+                                  sa_index *idx, void *stream);
+
+/*
  * Step 2: per-edge partials (kvouter_forward, forward.rs).
  *
  *   q             [tq, hq, head_dim] float32, 16-byte aligned
