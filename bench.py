@@ -358,7 +358,10 @@ def run_ours(args, rank, world, local_rank):
     fwd_gbs = acct["forward"] / (fwd_ms / 1e3) / 1e9
     step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
-    traffic = ncu_traffic("forward_cc.cu", args.workload)
+    decode_like = w.tq <= 2 * w.batch and w.head_dim == 128
+    fwd_file = "forward_dec.cu" if decode_like else "forward_cc.cu"
+    fwd_kernel = "forward_dec_kernel" if decode_like else "forward_cc_kernel"
+    traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", ""))
     value = world * w.tq * args.steps / elapsed_s
     dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"
     return {
@@ -377,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
         "step_frac_of_hbm": step_gbs / peak,
         "tflops": acct["flops"] / (ms_per_step / 1e3) / 1e12,
         "stages_ms": {"index": index_ms, "forward": fwd_ms, "combine": comb_ms},
-        "roofline": {"kernel": "forward_cc_kernel (sa_forward)", "bound": "hbm",
+        "roofline": {"kernel": f"{fwd_kernel} (sa_forward)", "bound": "hbm",
                      "achieved": fwd_gbs, "peak": peak, "unit": "GB/s",
                      "frac": fwd_gbs / peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": acct["forward"],

@@ -23,13 +23,14 @@ import numpy as np
 import torch
 
 from . import _native
-from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE,
-                      STATUS_NAMES)
+from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_CUDA_CORE_GENERAL,
+                      PATH_TENSOR_CORE, STATUS_NAMES)
 
 __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
            "sa_build_index_no_alloc", "sa_forward",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
-           "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE"]
+           "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
+           "PATH_CUDA_CORE_GENERAL"]
 
 
 class SAError(RuntimeError):

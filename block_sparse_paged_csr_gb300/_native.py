@@ -15,7 +15,7 @@ STATUS_NAMES = {
     10: "UNSUPPORTED", 11: "INVALID_ARGUMENT",
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL = 0, 1, 2, 3
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",

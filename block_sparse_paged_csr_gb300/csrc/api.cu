@@ -173,7 +173,8 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   if (path == SA_PATH_TENSOR_CORE) return SA_ERR_UNSUPPORTED;
-  if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE) return SA_ERR_INVALID_ARGUMENT;
+  if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL)
+    return SA_ERR_INVALID_ARGUMENT;
   if (!sa::forward_cc_supported(head_dim, block_size, kv_bf16)) return SA_ERR_UNSUPPORTED;
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
       !l_partial)
@@ -211,7 +212,15 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   a.m_partial = m_partial;
   a.l_partial = l_partial;
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
-  const cudaError_t err = sa::launch_forward_cc(a, static_cast<cudaStream_t>(stream));
+  // Decode-shaped problems (about one query per sequence, so few rows per
+  // work split) go to the pipelined kernel; the general kernel takes the rest.
+  const bool dec_ok =
+      sa::forward_dec_supported(head_dim, block_size, page_size, a.qhead, kv_bf16);
+  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
+  const bool use_dec = dec_ok && (path == SA_PATH_CUDA_CORE ||
+                                  (path == SA_PATH_AUTO && decode_like));
+  const cudaError_t err = use_dec ? sa::launch_forward_dec(a, static_cast<cudaStream_t>(stream))
+                                  : sa::launch_forward_cc(a, static_cast<cudaStream_t>(stream));
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }

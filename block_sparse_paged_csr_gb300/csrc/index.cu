@@ -169,63 +169,90 @@ index_segments_kernel(IndexArgs a, WorkspaceLayout lay, int nseg) {
   int64_t excl[3];
   block_scan3(v, excl, s.tot, s.warp_tot);
 
-  if (tid == 0) {
-    publish(seg_a + seg, seg_b + seg, kFlagAgg, s.tot[0], s.tot[1], s.tot[2]);
+  if (warp == 0) {
+    // Decoupled look-back, 32 predecessors per step: lane j reads segment
+    // (window end - j); the nearest one with an inclusive prefix ends the walk.
+    if (lane == 0) publish(seg_a + seg, seg_b + seg, kFlagAgg, s.tot[0], s.tot[1], s.tot[2]);
+    __syncwarp();
     int64_t pe = 0, pu = 0, ps = 0;
     bool ok = true;
-    for (int k = seg - 1; k >= 0 && ok; --k) {
+    for (int hi_k = seg - 1; hi_k >= 0; hi_k -= 32) {
+      const int k = hi_k - lane;
       uint64_t wa = 0, wb = 0;
-      uint32_t it = 0;
-      for (;;) {
-        wa = ld_acquire(seg_a + k);
-        if (wa & kFlagMask) {
-          wb = ld_acquire(seg_b + k);
-          if ((wb & kFlagMask) == (wa & kFlagMask)) break;
+      bool mine_ok = true;
+      if (k >= 0) {
+        uint32_t it = 0;
+        for (;;) {
+          wa = ld_acquire(seg_a + k);
+          if (wa & kFlagMask) {
+            wb = ld_acquire(seg_b + k);
+            if ((wb & kFlagMask) == (wa & kFlagMask)) break;
+          }
+          if (++it > kSpinLimit) {
+            mine_ok = false;
+            break;
+          }
+          __nanosleep(32);
         }
-        if (++it > kSpinLimit) {
-          ok = false;
-          break;
-        }
-        __nanosleep(64);
       }
-      if (!ok) break;
-      pe += static_cast<int64_t>(wa & kLow62);
-      pu += static_cast<int64_t>((wb >> 31) & kLow31);
-      ps += static_cast<int64_t>(wb & kLow31);
-      if ((wa & kFlagMask) == kFlagIncl) break;
-    }
-    if (!ok) report(status, SA_ERR_DEVICE_TIMEOUT);
-    s.prefix[0] = pe;
-    s.prefix[1] = pu;
-    s.prefix[2] = ps;
-    if (b == 0) {
-      // This segment opens head h: publish the head's bases before the
-      // inclusive flag so that later segments of the head can read them.
-      a.idx.edge_head_base[h] = pe;
-      head_units[h] = static_cast<int32_t>(pu);
-      s.head_edges = pe;
-      s.head_units = pu;
-    }
-    publish(seg_a + seg, seg_b + seg, kFlagIncl, pe + s.tot[0], pu + s.tot[1], ps + s.tot[2]);
-    if (b != 0) {
-      const int first = seg - b;
-      uint32_t it = 0;
-      while ((ld_acquire(seg_a + first) & kFlagMask) != kFlagIncl) {
-        if (++it > kSpinLimit) {
-          report(status, SA_ERR_DEVICE_TIMEOUT);
-          break;
-        }
-        __nanosleep(64);
+      if (!__all_sync(0xffffffffu, mine_ok)) {
+        ok = false;
+        break;
       }
-      s.head_edges = *reinterpret_cast<volatile int64_t*>(a.idx.edge_head_base + h);
-      s.head_units = *reinterpret_cast<volatile int32_t*>(head_units + h);
+      const unsigned incl =
+          __ballot_sync(0xffffffffu, k >= 0 && (wa & kFlagMask) == kFlagIncl);
+      const int stop = incl ? __ffs(incl) - 1 : 31;
+      int64_t ce = 0, cu_ = 0, cs = 0;
+      if (k >= 0 && lane <= stop) {
+        ce = static_cast<int64_t>(wa & kLow62);
+        cu_ = static_cast<int64_t>((wb >> 31) & kLow31);
+        cs = static_cast<int64_t>(wb & kLow31);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        ce += __shfl_xor_sync(0xffffffffu, ce, off);
+        cu_ += __shfl_xor_sync(0xffffffffu, cu_, off);
+        cs += __shfl_xor_sync(0xffffffffu, cs, off);
+      }
+      pe += ce;
+      pu += cu_;
+      ps += cs;
+      if (incl) break;
     }
-    if (b == a.batch - 1) a.idx.num_sel[h] = static_cast<int32_t>(pu + s.tot[1] - s.head_units);
-    if (seg == nseg - 1) {
-      a.idx.edge_head_base[a.hkv] = pe + s.tot[0];
-      a.idx.totals[0] = pe + s.tot[0];
-      a.idx.totals[1] = ps + s.tot[2];
-      a.idx.totals[2] = pu + s.tot[1];
+    if (lane == 0) {
+      if (!ok) report(status, SA_ERR_DEVICE_TIMEOUT);
+      s.prefix[0] = pe;
+      s.prefix[1] = pu;
+      s.prefix[2] = ps;
+      if (b == 0) {
+        // This segment opens head h: publish the head's bases before the
+        // inclusive flag so that later segments of the head can read them.
+        a.idx.edge_head_base[h] = pe;
+        head_units[h] = static_cast<int32_t>(pu);
+        s.head_edges = pe;
+        s.head_units = pu;
+      }
+      publish(seg_a + seg, seg_b + seg, kFlagIncl, pe + s.tot[0], pu + s.tot[1], ps + s.tot[2]);
+      if (b != 0) {
+        const int first = seg - b;
+        uint32_t it = 0;
+        while ((ld_acquire(seg_a + first) & kFlagMask) != kFlagIncl) {
+          if (++it > kSpinLimit) {
+            report(status, SA_ERR_DEVICE_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
+        s.head_edges = *reinterpret_cast<volatile int64_t*>(a.idx.edge_head_base + h);
+        s.head_units = *reinterpret_cast<volatile int32_t*>(head_units + h);
+      }
+      if (b == a.batch - 1) a.idx.num_sel[h] = static_cast<int32_t>(pu + s.tot[1] - s.head_units);
+      if (seg == nseg - 1) {
+        a.idx.edge_head_base[a.hkv] = pe + s.tot[0];
+        a.idx.totals[0] = pe + s.tot[0];
+        a.idx.totals[1] = ps + s.tot[2];
+        a.idx.totals[2] = pu + s.tot[1];
+      }
     }
   }
   __syncthreads();
@@ -288,7 +315,11 @@ index_segments_kernel(IndexArgs a, WorkspaceLayout lay, int nseg) {
     const int leader = __ffs(peers) - 1;
     const int wrank = __popc(peers & ((1u << lane) - 1u));
     int gbase = 0;
-    for (int w = 0; w < kWarps; ++w) {
+    // Warps take their running bin counts in warp order; warps past the
+    // chunk's last entry have nothing to take.
+    const int64_t left = n_seg - base;
+    const int active_warps = left >= kThreads ? kWarps : static_cast<int>((left + 31) >> 5);
+    for (int w = 0; w < active_warps; ++w) {
       if (warp == w && key >= 0 && lane == leader) {
         gbase = bins[key];
         bins[key] = gbase + __popc(peers);

@@ -62,6 +62,10 @@ struct ForwardArgs {
 cudaError_t launch_forward_cc(const ForwardArgs& a, cudaStream_t stream);
 bool forward_cc_supported(int head_dim, int block_size, int kv_bf16);
 
+// Pipelined decode-shaped forward (head_dim 128, few rows per split).
+cudaError_t launch_forward_dec(const ForwardArgs& a, cudaStream_t stream);
+bool forward_dec_supported(int head_dim, int block_size, int page_size, int qhead, int kv_bf16);
+
 struct CombineArgs {
   const int32_t* inv;
   const int64_t* edge_head_base;

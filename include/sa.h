@@ -63,9 +63,11 @@ typedef enum sa_dtype {
 
 /* Forward kernel choice (sa_forward / sa_attention `path`). */
 typedef enum sa_path {
-  SA_PATH_AUTO = 0,          /* pick per problem shape                          */
-  SA_PATH_CUDA_CORE = 1,     /* f32 FMA kernel, any supported shape             */
-  SA_PATH_TENSOR_CORE = 2    /* tcgen05 kernel; SA_ERR_UNSUPPORTED where absent */
+  SA_PATH_AUTO = 0,              /* pick per problem shape                          */
+  SA_PATH_CUDA_CORE = 1,         /* f32 FMA kernels: the pipelined decode kernel
+                                    where its shape limits allow, else the general one */
+  SA_PATH_TENSOR_CORE = 2,       /* tcgen05 kernel; SA_ERR_UNSUPPORTED where absent */
+  SA_PATH_CUDA_CORE_GENERAL = 3  /* the general f32 FMA kernel only                 */
 } sa_path;
 
 /*

@@ -189,3 +189,41 @@ def test_full_size_workload(name):
     _gpu.compare_lse(lse[rows[:, 0], rows[:, 1]].cpu().numpy(), ref_lse, _gpu.TOL_F32)
     del t
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- each kernel
+
+
+def _check_against_oracle(w, t, split, path, tol=_gpu.TOL_F32):
+    out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=split, path=path)
+    ref_out, ref_lse, ref_idx, (ro, rm, rl) = _oracle_attention(w, split)
+    _gpu.compare_index(idx.to_host(), ref_idx)
+    rows = ref_idx["edges"].shape[0] * w.qhead
+    _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(), l[:rows].cpu().numpy(),
+                          ro, rm, rl, tol)
+    assert _gpu.row_error(out.cpu().numpy(), ref_out) <= tol
+    _gpu.compare_lse(lse.cpu().numpy(), ref_lse, tol)
+
+
+@pytest.mark.parametrize("split", [0, 2])
+@pytest.mark.parametrize("path", [sa.PATH_CUDA_CORE, sa.PATH_CUDA_CORE_GENERAL],
+                         ids=["cuda_core", "cuda_core_general"])
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workload_each_cuda_core_kernel(name, path, split):
+    """PATH_CUDA_CORE runs the pipelined decode kernel wherever its limits
+    allow (head_dim 128), including multi-edge splits (row groups);
+    PATH_CUDA_CORE_GENERAL the general kernel."""
+    w = inputs.small(name, seed=1)
+    _check_against_oracle(w, _gpu.device_workload(w), split, path)
+
+
+@pytest.mark.parametrize("bs,ps,qhead,dt", [(32, 16, 1, "f32"), (64, 16, 2, "bf16"),
+                                            (128, 64, 8, "f32"), (128, 16, 8, "bf16"),
+                                            (64, 8, 4, "f32"), (32, 4, 4, "bf16"),
+                                            (64, 16, 8, "f32"), (128, 32, 4, "bf16")])
+def test_decode_kernel_shapes(bs, ps, qhead, dt):
+    w = inputs.gqa_decode(seed=bs + ps + qhead, batch=7, kv_min=900, kv_max=2100, hkv=2,
+                          hq=2 * qhead, head_dim=128, page_size=ps, block_size=bs, topk=6,
+                          kv_dtype=dt)
+    w.block_tables[1, 3] = -1          # a hole inside a live block
+    _check_against_oracle(w, _gpu.device_workload(w), 0, sa.PATH_CUDA_CORE)
