@@ -99,7 +99,9 @@ sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t ba
   out->inv = n;
   out->splits = 4 * n;
   out->totals = 4;
-  out->workspace_bytes = sa::workspace_layout(hkv, batch).total;
+  out->workspace_bytes =
+      sa::workspace_layout(hkv, batch, sa::index_hist_slot_bound(tq, topk), static_cast<int32_t>(msb))
+          .total;
   return SA_OK;
 }
 
@@ -124,7 +126,11 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   if (!aligned16(idx->splits) || !aligned16(idx->edges) ||
       (reinterpret_cast<uintptr_t>(idx->workspace) & 255u) != 0)
     return SA_ERR_INVALID_ARGUMENT;
-  const sa::WorkspaceLayout lay = sa::workspace_layout(hkv, batch);
+  int64_t multi_slots = 0;
+  const int64_t chunks_per_head =
+      sa::index_chunks_per_head(cu_seqlens_q_host, batch, topk, &multi_slots);
+  const sa::WorkspaceLayout lay =
+      sa::workspace_layout(hkv, batch, multi_slots, static_cast<int32_t>(msb));
   if (idx->workspace_bytes < lay.total) return SA_ERR_INVALID_ARGUMENT;
 
   idx->tq = tq;
@@ -152,7 +158,9 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   a.split_edges = split_edges;
   a.nbs = nbs;
   a.idx = *idx;
-  const cudaError_t err = sa::launch_build_index(a, static_cast<cudaStream_t>(stream));
+  const cudaError_t err =
+      sa::launch_build_index(a, chunks_per_head, multi_slots, static_cast<cudaStream_t>(stream));
+  if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 

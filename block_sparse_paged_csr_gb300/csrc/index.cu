@@ -1,22 +1,30 @@
 // Step 1 of KV-outer sparse attention: the CSR index (KvOuterIndex, types.rs
 // of alice-llm's sparse_attention) and the forward's work list (WorkSplit).
 //
-// Structure.  Entries (query i, kv head h, rank r) that belong to one
-// (h, sequence b) segment can only land in the raw slots b*msb .. b*msb+msb-1
-// of head h, and segments in (h, b) order own consecutive slot ranges.  So one
-// CTA per segment:
-//   1. histograms its entries into msb shared-memory bins (validating ids);
-//   2. scans the bins, publishes its totals and reads the totals of all
-//      earlier segments with a decoupled look-back (segments are handed out
-//      by an atomic ticket, so every segment it waits on is already running;
-//      every wait is bounded);
-//   3. writes sel_slots / sel_offsets / the split list for its non-empty bins;
-//   4. scatters its edges: entries walk in (query, rank) order, 512 at a time;
-//      a warp's equal keys are ranked with __match_any_sync, warps take their
-//      running bin counts in warp order, so the order inside every bucket is
-//      (query, rank) ascending and the result is deterministic.
-// A second small kernel writes the plateau (sel_offsets past num_sel[h]) and
-// the -1 padding of sel_slots, which need each head's final totals.
+// Structure.  The entries (query i, kv head h, rank r) of one (h, sequence b)
+// segment can only land in raw slots b*msb .. b*msb+msb-1 of head h, and
+// segments in (h, b) order own consecutive slot ranges.  A segment's entries
+// in (query, rank) order are cut into chunks of at most kChunkEntries; CTAs
+// walk chunks with a grid stride.  One cooperative kernel, two phases:
+//   phase 1  each chunk histograms its entries into msb shared-memory bins;
+//            a one-chunk segment writes its totals (edges, non-empty bins,
+//            work splits) directly; a segment of several chunks stores each
+//            chunk's histogram, and the chunk that arrives last (atomic
+//            counter after a fence) sums them and writes the totals.
+//   -- one grid barrier (bounded spin; the launch is cooperative, so every
+//      CTA is resident); the last CTA to arrive scans the segment totals
+//      into exclusive prefixes before it releases the others --
+//   phase 2  each chunk reads its segment's global prefix and its head's
+//            base, rebuilds its bins, scans them, and (first chunk of the
+//            segment) writes sel_slots / sel_offsets / the splits of the
+//            segment; then it scatters its own edges: entries walk in
+//            (query, rank) order 256 at a time, equal keys inside a warp are
+//            ranked with
+//            __match_any_sync and warps take their running bin counts in warp
+//            order, on top of the counts of the segment's earlier chunks, so
+//            each bucket is in ascending (query, rank) order and the result
+//            is deterministic.  All CTAs then write the plateau of
+//            sel_offsets and the -1 padding of sel_slots.
 #include <algorithm>
 #include <cstdint>
 
@@ -27,31 +35,17 @@ namespace sa {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr uint64_t kFlagAgg = 1ull << 62;
-constexpr uint64_t kFlagIncl = 2ull << 62;
-constexpr uint64_t kFlagMask = 3ull << 62;
-constexpr uint64_t kLow31 = (1ull << 31) - 1;
-constexpr uint64_t kLow62 = (1ull << 62) - 1;
 
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Segment status: word A = flag | edges, word B = flag | units << 31 | splits.
-// B is stored before A, each with release order; a reader accepts a pair only
-// when both carry the same flag.
-__device__ __forceinline__ void publish(uint64_t* a, uint64_t* b, uint64_t flag, int64_t edges,
-                                        int64_t units, int64_t splits) {
-  st_release(b, flag | (static_cast<uint64_t>(units) << 31) | static_cast<uint64_t>(splits));
-  st_release(a, flag | static_cast<uint64_t>(edges));
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int64_t splits_of(int64_t count, int split_edges) {
@@ -60,7 +54,68 @@ __device__ __forceinline__ int64_t splits_of(int64_t count, int split_edges) {
   return (count + split_edges - 1) / split_edges;
 }
 
-// Exclusive block scan of three values; also returns the block totals.
+// Grid-wide barrier for a cooperative launch.  The last CTA to arrive first
+// runs `last` (with all of its threads), then resets the counter and bumps the
+// generation; the others spin (bounded) on the generation.
+template <typename F>
+__device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, F last) {
+  __shared__ int s_ok, s_last;
+  __shared__ uint32_t s_gen;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_ok = 1;
+    s_gen = ld_acquire_u32(gen);
+    __threadfence();
+    s_last = atomicAdd(count, 1u) == nblocks - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    last();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      atomicExch(count, 0u);
+      __threadfence();
+      st_release_u32(gen, s_gen + 1);
+    }
+  } else if (threadIdx.x == 0) {
+    uint32_t it = 0;
+    while (ld_acquire_u32(gen) == s_gen) {
+      if (++it > kSpinLimit) {
+        s_ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Block-wide sum of three 64-bit values; every thread gets the totals.
+__device__ __forceinline__ void block_sum3(int64_t v[3], int64_t (*scratch)[kWarps]) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int q = 0; q < 3; ++q) scratch[q][warp] = v[q];
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    int64_t t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += scratch[q][w];
+    v[q] = t;
+  }
+}
+
+// Exclusive block scan of three values (per-thread contributions in thread
+// order); also returns the block totals.
 __device__ __forceinline__ void block_scan3(int64_t v[3], int64_t excl[3], int64_t tot[3],
                                             int64_t (*warp_tot)[kWarps]) {
   const int lane = threadIdx.x & 31;
@@ -74,329 +129,450 @@ __device__ __forceinline__ void block_scan3(int64_t v[3], int64_t excl[3], int64
       if (lane >= off) inc[q] += n;
     }
   }
-  if (lane == 31) {
+  __syncthreads();
+  if (lane == 31)
 #pragma unroll
     for (int q = 0; q < 3; ++q) warp_tot[q][warp] = inc[q];
-  }
   __syncthreads();
-  if (warp == 0) {
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      int64_t x = lane < kWarps ? warp_tot[q][lane] : 0;
-      int64_t y = x;
+  for (int q = 0; q < 3; ++q) {
+    int64_t before = 0, all = 0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int64_t n = __shfl_up_sync(0xffffffffu, y, off);
-        if (lane >= off) y += n;
-      }
-      if (lane < kWarps) warp_tot[q][lane] = y - x;   // exclusive over warps
-      const int64_t all = __shfl_sync(0xffffffffu, y, 31);
-      if (lane == 0) tot[q] = all;
+    for (int w = 0; w < kWarps; ++w) {
+      const int64_t x = warp_tot[q][w];
+      if (w < warp) before += x;
+      all += x;
     }
+    excl[q] = before + inc[q] - v[q];
+    tot[q] = all;
   }
-  __syncthreads();
-#pragma unroll
-  for (int q = 0; q < 3; ++q) excl[q] = warp_tot[q][warp] + inc[q] - v[q];
 }
 
-struct SegShared {
-  int64_t warp_tot[3][kWarps];
-  int64_t tot[3];
-  int64_t prefix[3];      // global exclusive prefix: edges, units, splits
-  int64_t head_edges;     // global edge index of the head's first edge
-  int64_t head_units;     // global unit index of the head's first unit
-  int seg;
+struct Shared {
+  int64_t scratch[3][kWarps];
+  int32_t nch_head;      // chunks per head
+  int32_t nmulti_head;   // histogram slots per head
+  int last;
 };
 
-__global__ void __launch_bounds__(kThreads)
-index_segments_kernel(IndexArgs a, WorkspaceLayout lay, int nseg) {
-  extern __shared__ int32_t dyn[];
-  int32_t* bins = dyn;                // [msb] counts, later running counters
-  int32_t* start = dyn + a.msb;       // [msb] global edge index of each bin's first edge
-  __shared__ SegShared s;
+// Which (head, sequence, chunk) a chunk id names.
+__device__ __forceinline__ void locate(int64_t c, const int32_t* chunk_base, int batch,
+                                       int nch_head, int& h, int& b, int& k) {
+  h = static_cast<int>(c / nch_head);
+  const int r = static_cast<int>(c - static_cast<int64_t>(h) * nch_head);
+  int lo = 0, hi = batch;   // largest b with chunk_base[b] <= r and a chunk
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (chunk_base[mid] <= r) lo = mid; else hi = mid;
+  }
+  b = lo;
+  k = r - chunk_base[lo];
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
+  extern __shared__ int64_t dyn64[];
+  const int msb = a.msb;
+  const int batch = a.batch;
+  int64_t* head_tot = dyn64;                                          // [hkv][2]
+  int32_t* bins = reinterpret_cast<int32_t*>(dyn64 + 2 * a.hkv);      // [msb]
+  int32_t* before = bins + msb;                                       // [msb]
+  int32_t* start = before + msb;                                      // [msb]
+  int32_t* chunk_base = start + msb;                                  // [batch+1]
+  int32_t* multi_base = chunk_base + batch + 1;                       // [batch+1]
+  __shared__ Shared s;
 
   char* ws = static_cast<char*>(a.idx.workspace);
-  uint32_t* ticket = reinterpret_cast<uint32_t*>(ws + lay.ticket);
-  uint64_t* seg_a = reinterpret_cast<uint64_t*>(ws + lay.seg_a);
-  uint64_t* seg_b = reinterpret_cast<uint64_t*>(ws + lay.seg_b);
-  int32_t* head_units = reinterpret_cast<int32_t*>(ws + lay.head_units);
+  uint32_t* bar_count = reinterpret_cast<uint32_t*>(ws + lay.barrier);
+  uint32_t* bar_gen = bar_count + 1;
+  uint32_t* seg_done = reinterpret_cast<uint32_t*>(ws + lay.seg_done);
+  int32_t* seg_tot = reinterpret_cast<int32_t*>(ws + lay.seg_tot);   // [nseg][3]
+  int64_t* seg_pre = reinterpret_cast<int64_t*>(ws + lay.seg_pre);   // [nseg+1][3] exclusive
+  int32_t* hist = reinterpret_cast<int32_t*>(ws + lay.hist);         // [slots][msb]
   int64_t* status = a.idx.totals + 3;
-
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  if (tid == 0) s.seg = static_cast<int>(atomicAdd(ticket, 1u));
-  __syncthreads();
-  const int seg = s.seg;
-  if (seg >= nseg) return;  // cannot happen: the grid has exactly nseg CTAs
-  const int h = seg / a.batch;
-  const int b = seg % a.batch;
-  const int msb = a.msb;
   const int topk = a.topk;
-  const int64_t q0 = a.cu[b];
-  const int64_t qo = a.cu[b + 1] - q0;
-  const int64_t lk = a.used ? (a.used[b] > 0 ? a.used[b] : 0)
-                            : static_cast<int64_t>(msb) * a.block_size;
-  const int64_t n_seg = qo > 0 ? qo * topk : 0;
   const int32_t* sel = a.selected;
+  const int64_t cap = a.tq * a.hkv * static_cast<int64_t>(topk);
+  const int nseg = a.hkv * batch;
 
-  // ---- 1. histogram -------------------------------------------------------
-  for (int k = tid; k < msb; k += kThreads) bins[k] = 0;
-  __syncthreads();
-  for (int64_t e = tid; e < n_seg; e += kThreads) {
-    const int64_t i = q0 + e / topk;
-    const int r = static_cast<int>(e % topk);
-    const int blk = sel[(i * a.hkv + h) * topk + r];
-    if (blk < -1 || blk >= msb) {
-      report(status, SA_ERR_SELECTED_RANGE);
-      continue;
+  // ---- chunk table (every CTA builds its own copy) -------------------------
+  if (tid == 0) {
+    int32_t c = 0, m = 0;
+    for (int b = 0; b < batch; ++b) {
+      chunk_base[b] = c;
+      multi_base[b] = m;
+      const int64_t n = (a.cu[b + 1] - a.cu[b]) * topk;
+      const int32_t nc = static_cast<int32_t>((n + kChunkEntries - 1) / kChunkEntries);
+      c += nc;
+      if (nc > 1) m += nc;
     }
-    if (blk >= 0 && static_cast<int64_t>(blk) * a.block_size < lk) atomicAdd(&bins[blk], 1);
+    chunk_base[batch] = c;
+    multi_base[batch] = m;
+    s.nch_head = c;
+    s.nmulti_head = m;
   }
+  if (blockIdx.x == 0 && tid == 0) *status = 0;
   __syncthreads();
+  const int nch_head = s.nch_head;
+  const int nmulti = s.nmulti_head;
 
-  // ---- 2. local scan + look-back -------------------------------------------
-  const int per = (msb + kThreads - 1) / kThreads;
-  const int lo = min(tid * per, msb);
-  const int hi = min(lo + per, msb);
-  int64_t v[3] = {0, 0, 0};
-  for (int k = lo; k < hi; ++k) {
-    const int c = bins[k];
-    v[0] += c;
-    v[1] += c > 0;
-    v[2] += splits_of(c, a.split_edges);
-  }
-  int64_t excl[3];
-  block_scan3(v, excl, s.tot, s.warp_tot);
-
-  if (warp == 0) {
-    // Decoupled look-back, 32 predecessors per step: lane j reads segment
-    // (window end - j); the nearest one with an inclusive prefix ends the walk.
-    if (lane == 0) publish(seg_a + seg, seg_b + seg, kFlagAgg, s.tot[0], s.tot[1], s.tot[2]);
-    __syncwarp();
-    int64_t pe = 0, pu = 0, ps = 0;
-    bool ok = true;
-    for (int hi_k = seg - 1; hi_k >= 0; hi_k -= 32) {
-      const int k = hi_k - lane;
-      uint64_t wa = 0, wb = 0;
-      bool mine_ok = true;
-      if (k >= 0) {
-        uint32_t it = 0;
-        for (;;) {
-          wa = ld_acquire(seg_a + k);
-          if (wa & kFlagMask) {
-            wb = ld_acquire(seg_b + k);
-            if ((wb & kFlagMask) == (wa & kFlagMask)) break;
-          }
-          if (++it > kSpinLimit) {
-            mine_ok = false;
-            break;
-          }
-          __nanosleep(32);
-        }
-      }
-      if (!__all_sync(0xffffffffu, mine_ok)) {
-        ok = false;
-        break;
-      }
-      const unsigned incl =
-          __ballot_sync(0xffffffffu, k >= 0 && (wa & kFlagMask) == kFlagIncl);
-      const int stop = incl ? __ffs(incl) - 1 : 31;
-      int64_t ce = 0, cu_ = 0, cs = 0;
-      if (k >= 0 && lane <= stop) {
-        ce = static_cast<int64_t>(wa & kLow62);
-        cu_ = static_cast<int64_t>((wb >> 31) & kLow31);
-        cs = static_cast<int64_t>(wb & kLow31);
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        ce += __shfl_xor_sync(0xffffffffu, ce, off);
-        cu_ += __shfl_xor_sync(0xffffffffu, cu_, off);
-        cs += __shfl_xor_sync(0xffffffffu, cs, off);
-      }
-      pe += ce;
-      pu += cu_;
-      ps += cs;
-      if (incl) break;
-    }
-    if (lane == 0) {
-      if (!ok) report(status, SA_ERR_DEVICE_TIMEOUT);
-      s.prefix[0] = pe;
-      s.prefix[1] = pu;
-      s.prefix[2] = ps;
-      if (b == 0) {
-        // This segment opens head h: publish the head's bases before the
-        // inclusive flag so that later segments of the head can read them.
-        a.idx.edge_head_base[h] = pe;
-        head_units[h] = static_cast<int32_t>(pu);
-        s.head_edges = pe;
-        s.head_units = pu;
-      }
-      publish(seg_a + seg, seg_b + seg, kFlagIncl, pe + s.tot[0], pu + s.tot[1], ps + s.tot[2]);
-      if (b != 0) {
-        const int first = seg - b;
-        uint32_t it = 0;
-        while ((ld_acquire(seg_a + first) & kFlagMask) != kFlagIncl) {
-          if (++it > kSpinLimit) {
-            report(status, SA_ERR_DEVICE_TIMEOUT);
-            break;
-          }
-          __nanosleep(32);
-        }
-        s.head_edges = *reinterpret_cast<volatile int64_t*>(a.idx.edge_head_base + h);
-        s.head_units = *reinterpret_cast<volatile int32_t*>(head_units + h);
-      }
-      if (b == a.batch - 1) a.idx.num_sel[h] = static_cast<int32_t>(pu + s.tot[1] - s.head_units);
-      if (seg == nseg - 1) {
-        a.idx.edge_head_base[a.hkv] = pe + s.tot[0];
-        a.idx.totals[0] = pe + s.tot[0];
-        a.idx.totals[1] = ps + s.tot[2];
-        a.idx.totals[2] = pu + s.tot[1];
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- 3. compact slots and work splits ------------------------------------
-  const int64_t cap = static_cast<int64_t>(a.tq) * a.hkv * topk;  // edges / splits capacity
-  {
-    int64_t ge = s.prefix[0] + excl[0];
-    int64_t gu = s.prefix[1] + excl[1];
-    int64_t gs = s.prefix[2] + excl[2];
-    const int64_t nbs = a.nbs;
-    for (int k = lo; k < hi; ++k) {
-      const int c = bins[k];
-      start[k] = static_cast<int32_t>(ge);
-      if (c > 0) {
-        const int64_t j = gu - s.head_units;
-        if (j >= 0 && j < nbs) {
-          a.idx.sel_slots[h * nbs + j] = static_cast<int32_t>(static_cast<int64_t>(b) * msb + k);
-          a.idx.sel_offsets[h * (nbs + 1) + j] = static_cast<int32_t>(ge - s.head_edges);
-        }
-        const int step = a.split_edges > 0 ? a.split_edges : c;
-        const int64_t nsp = splits_of(c, a.split_edges);
-        for (int64_t t = 0; t < nsp; ++t) {
-          const int64_t g = gs + t;
-          if (g < cap) {
-            const int64_t e_lo = ge + t * step;
-            const int64_t e_hi = min(e_lo + step, ge + c);
-            int4 w;
-            w.x = h;
-            w.y = static_cast<int32_t>(j);
-            w.z = static_cast<int32_t>(e_lo);
-            w.w = static_cast<int32_t>(e_hi);
-            reinterpret_cast<int4*>(a.idx.splits)[g] = w;
-          }
-        }
-        gs += nsp;
-        gu += 1;
-      }
-      ge += c;
-    }
-  }
-  __syncthreads();
-  for (int k = tid; k < msb; k += kThreads) bins[k] = 0;
-  __syncthreads();
-
-  // ---- 4. stable scatter of edges and inv ----------------------------------
-  const int64_t head_edges = s.head_edges;
-  for (int64_t base = 0; base < n_seg; base += kThreads) {
-    const int64_t e = base + tid;
-    int key = -1;
-    int64_t i = 0;
-    int r = 0;
-    if (e < n_seg) {
-      i = q0 + e / topk;
-      r = static_cast<int>(e % topk);
+  // ---- phase 1: per-chunk histograms and segment totals ---------------------
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    int h, b, k;
+    locate(c, chunk_base, batch, nch_head, h, b, k);
+    const int nc = chunk_base[b + 1] - chunk_base[b];
+    const int64_t q0 = a.cu[b];
+    const int64_t n_seg = (a.cu[b + 1] - q0) * topk;
+    const int64_t e0 = static_cast<int64_t>(k) * kChunkEntries;
+    const int64_t e1 = min(n_seg, e0 + kChunkEntries);
+    const int64_t lk = a.used ? (a.used[b] > 0 ? a.used[b] : 0)
+                              : static_cast<int64_t>(msb) * a.block_size;
+    for (int t = tid; t < msb; t += kThreads) bins[t] = 0;
+    __syncthreads();
+    for (int64_t e = e0 + tid; e < e1; e += kThreads) {
+      const int64_t i = q0 + e / topk;
+      const int r = static_cast<int>(e % topk);
       const int blk = sel[(i * a.hkv + h) * topk + r];
-      if (blk >= 0 && blk < msb && static_cast<int64_t>(blk) * a.block_size < lk) key = blk;
+      if (blk >= 0 && blk < msb && static_cast<int64_t>(blk) * a.block_size < lk)
+        atomicAdd(&bins[blk], 1);
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int leader = __ffs(peers) - 1;
-    const int wrank = __popc(peers & ((1u << lane) - 1u));
-    int gbase = 0;
-    // Warps take their running bin counts in warp order; warps past the
-    // chunk's last entry have nothing to take.
-    const int64_t left = n_seg - base;
-    const int active_warps = left >= kThreads ? kWarps : static_cast<int>((left + 31) >> 5);
-    for (int w = 0; w < active_warps; ++w) {
-      if (warp == w && key >= 0 && lane == leader) {
-        gbase = bins[key];
-        bins[key] = gbase + __popc(peers);
-      }
+    __syncthreads();
+    const int seg = h * batch + b;
+    bool totals_here = nc == 1;
+    if (nc > 1) {
+      int32_t* mine = hist + (static_cast<int64_t>(h) * nmulti + multi_base[b] + k) * msb;
+      for (int t = tid; t < msb; t += kThreads) mine[t] = bins[t];
+      __threadfence();
       __syncthreads();
-    }
-    gbase = __shfl_sync(0xffffffffu, gbase, leader);
-    if (e < n_seg) {
-      const int64_t inv_at = (static_cast<int64_t>(h) * a.tq + i) * topk + r;
-      if (key >= 0) {
-        const int64_t pos = static_cast<int64_t>(start[key]) + gbase + wrank;
-        if (pos >= 0 && pos < cap) {
-          reinterpret_cast<int2*>(a.idx.edges)[pos] = make_int2(static_cast<int32_t>(i), r);
-          a.idx.inv[inv_at] = static_cast<int32_t>(pos - head_edges);
+      if (tid == 0) s.last = atomicAdd(seg_done + seg, 1u) == static_cast<uint32_t>(nc - 1);
+      __syncthreads();
+      totals_here = s.last != 0;
+      if (totals_here) {
+        __threadfence();
+        const int32_t* first = hist + (static_cast<int64_t>(h) * nmulti + multi_base[b]) * msb;
+        for (int t = tid; t < msb; t += kThreads) {
+          int32_t sum = 0;
+          for (int kk = 0; kk < nc; ++kk)
+            sum += *reinterpret_cast<const volatile int32_t*>(first + static_cast<int64_t>(kk) * msb + t);
+          bins[t] = sum;
         }
-      } else {
-        a.idx.inv[inv_at] = -1;
+        __syncthreads();
       }
+    }
+    if (totals_here) {
+      int64_t v[3] = {0, 0, 0};
+      for (int t = tid; t < msb; t += kThreads) {
+        const int cnt = bins[t];
+        v[0] += cnt;
+        v[1] += cnt > 0;
+        v[2] += splits_of(cnt, a.split_edges);
+      }
+      block_sum3(v, s.scratch);
+      if (tid == 0) {
+        seg_tot[3 * seg + 0] = static_cast<int32_t>(v[0]);
+        seg_tot[3 * seg + 1] = static_cast<int32_t>(v[1]);
+        seg_tot[3 * seg + 2] = static_cast<int32_t>(v[2]);
+      }
+    }
+    __syncthreads();
+  }
+  // Segments without entries have no chunk: their totals are zero.
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < nseg;
+       g += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int b = static_cast<int>(g % batch);
+    if (chunk_base[b + 1] == chunk_base[b]) {
+      seg_tot[3 * g + 0] = 0;
+      seg_tot[3 * g + 1] = 0;
+      seg_tot[3 * g + 2] = 0;
+    }
+  }
+
+  __threadfence();
+  // The last CTA to finish phase 1 turns the segment totals into exclusive
+  // prefixes (edges, non-empty bins, splits) for everyone.
+  auto scan_segments = [&]() {
+    int64_t carry[3] = {0, 0, 0};
+    for (int base = 0; base < nseg; base += kThreads) {
+      const int q = base + tid;
+      int64_t v[3] = {0, 0, 0};
+      if (q < nseg)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) v[j] = *reinterpret_cast<volatile int32_t*>(seg_tot + 3 * q + j);
+      int64_t excl[3], tot[3];
+      block_scan3(v, excl, tot, s.scratch);
+      if (q < nseg)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) seg_pre[3 * q + j] = carry[j] + excl[j];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) carry[j] += tot[j];
+    }
+    if (tid == 0)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) seg_pre[3 * nseg + j] = carry[j];
+    __threadfence();
+  };
+  if (!grid_barrier(bar_count, bar_gen, gridDim.x, scan_segments)) {
+    if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+    return;
+  }
+  // Per-head totals of edges and non-empty bins.
+  for (int h = tid; h < a.hkv; h += kThreads) {
+    const volatile int64_t* lo = seg_pre + 3 * static_cast<int64_t>(h) * batch;
+    const volatile int64_t* hi = seg_pre + 3 * static_cast<int64_t>(h + 1) * batch;
+    head_tot[2 * h + 0] = hi[0] - lo[0];
+    head_tot[2 * h + 1] = hi[1] - lo[1];
+  }
+  __syncthreads();
+
+  // ---- phase 2: prefixes, slot writes, stable scatter ----------------------
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    int h, b, k;
+    locate(c, chunk_base, batch, nch_head, h, b, k);
+    const int nc = chunk_base[b + 1] - chunk_base[b];
+    const int seg = h * batch + b;
+    const int64_t q0 = a.cu[b];
+    const int64_t n_seg = (a.cu[b + 1] - q0) * topk;
+    const int64_t e0 = static_cast<int64_t>(k) * kChunkEntries;
+    const int64_t e1 = min(n_seg, e0 + kChunkEntries);
+    const int64_t lk = a.used ? (a.used[b] > 0 ? a.used[b] : 0)
+                              : static_cast<int64_t>(msb) * a.block_size;
+    // Global exclusive prefix of this segment, and its head's base.
+    int64_t pre[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) pre[j] = *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * seg + j);
+    const int64_t head_edges =
+        *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 0);
+    const int64_t head_units =
+        *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 1);
+    // This chunk's bins (validating ids) and the counts of earlier chunks.
+    for (int t = tid; t < msb; t += kThreads) {
+      bins[t] = 0;
+      before[t] = 0;
+    }
+    __syncthreads();
+    for (int64_t e = e0 + tid; e < e1; e += kThreads) {
+      const int64_t i = q0 + e / topk;
+      const int r = static_cast<int>(e % topk);
+      const int blk = sel[(i * a.hkv + h) * topk + r];
+      if (blk < -1 || blk >= msb) {
+        report(status, SA_ERR_SELECTED_RANGE);
+        continue;
+      }
+      if (blk >= 0 && static_cast<int64_t>(blk) * a.block_size < lk) atomicAdd(&bins[blk], 1);
+    }
+    __syncthreads();
+    if (nc > 1) {
+      // Segment totals per bin (into `start` for the scan) and the counts of
+      // the segment's earlier chunks (into `before`).
+      const int32_t* first = hist + (static_cast<int64_t>(h) * nmulti + multi_base[b]) * msb;
+      for (int t = tid; t < msb; t += kThreads) {
+        int32_t sum = 0, bef = 0;
+        for (int kk = 0; kk < nc; ++kk) {
+          const int32_t x = first[static_cast<int64_t>(kk) * msb + t];
+          sum += x;
+          if (kk < k) bef += x;
+        }
+        start[t] = sum;
+        before[t] = bef;
+      }
+    } else {
+      for (int t = tid; t < msb; t += kThreads) start[t] = bins[t];
+    }
+    __syncthreads();
+    // Scan of the segment's bins; slot outputs from the segment's first chunk.
+    const int per = (msb + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, msb);
+    const int hi = min(lo + per, msb);
+    int64_t v[3] = {0, 0, 0};
+    for (int t = lo; t < hi; ++t) {
+      const int cnt = start[t];
+      v[0] += cnt;
+      v[1] += cnt > 0;
+      v[2] += splits_of(cnt, a.split_edges);
+    }
+    int64_t excl[3], tot[3];
+    block_scan3(v, excl, tot, s.scratch);
+    {
+      int64_t ge = pre[0] + excl[0];
+      int64_t gu = pre[1] + excl[1];
+      int64_t gs = pre[2] + excl[2];
+      const int64_t nbs = a.nbs;
+      for (int t = lo; t < hi; ++t) {
+        const int cnt = start[t];
+        if (k == 0 && cnt > 0) {
+          const int64_t j = gu - head_units;
+          if (j >= 0 && j < nbs) {
+            a.idx.sel_slots[h * nbs + j] = static_cast<int32_t>(static_cast<int64_t>(b) * msb + t);
+            a.idx.sel_offsets[h * (nbs + 1) + j] = static_cast<int32_t>(ge - head_edges);
+          }
+          const int step = a.split_edges > 0 ? a.split_edges : cnt;
+          const int64_t nsp = splits_of(cnt, a.split_edges);
+          for (int64_t u = 0; u < nsp; ++u) {
+            const int64_t g = gs + u;
+            if (g < cap) {
+              const int64_t lo_e = ge + u * step;
+              int4 w;
+              w.x = h;
+              w.y = static_cast<int32_t>(j);
+              w.z = static_cast<int32_t>(lo_e);
+              w.w = static_cast<int32_t>(min(lo_e + step, ge + cnt));
+              reinterpret_cast<int4*>(a.idx.splits)[g] = w;
+            }
+          }
+        }
+        gs += splits_of(cnt, a.split_edges);
+        gu += cnt > 0;
+        before[t] = static_cast<int32_t>(ge) + before[t];   // first edge of this chunk's entries
+        ge += cnt;
+      }
+    }
+    __syncthreads();
+    for (int t = tid; t < msb; t += kThreads) bins[t] = 0;
+    __syncthreads();
+    for (int64_t base = e0; base < e1; base += kThreads) {
+      const int64_t e = base + tid;
+      int key = -1;
+      int64_t i = 0;
+      int r = 0;
+      if (e < e1) {
+        i = q0 + e / topk;
+        r = static_cast<int>(e % topk);
+        const int blk = sel[(i * a.hkv + h) * topk + r];
+        if (blk >= 0 && blk < msb && static_cast<int64_t>(blk) * a.block_size < lk) key = blk;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const int leader = __ffs(peers) - 1;
+      const int wrank = __popc(peers & ((1u << lane) - 1u));
+      int gbase = 0;
+      // Warps take their running bin counts in warp order; warps past the
+      // chunk's last entry have nothing to take.
+      const int64_t left = e1 - base;
+      const int active = left >= kThreads ? kWarps : static_cast<int>((left + 31) >> 5);
+      for (int w = 0; w < active; ++w) {
+        if (warp == w && key >= 0 && lane == leader) {
+          gbase = bins[key];
+          bins[key] = gbase + __popc(peers);
+        }
+        __syncthreads();
+      }
+      gbase = __shfl_sync(0xffffffffu, gbase, leader);
+      if (e < e1) {
+        const int64_t inv_at = (static_cast<int64_t>(h) * a.tq + i) * topk + r;
+        if (key >= 0) {
+          const int64_t pos = static_cast<int64_t>(before[key]) + gbase + wrank;
+          if (pos >= 0 && pos < cap) {
+            reinterpret_cast<int2*>(a.idx.edges)[pos] = make_int2(static_cast<int32_t>(i), r);
+            a.idx.inv[inv_at] = static_cast<int32_t>(pos - head_edges);
+          }
+        } else {
+          a.idx.inv[inv_at] = -1;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- head-level outputs and the plateau -----------------------------------
+  if (blockIdx.x == 0) {
+    for (int h = tid; h <= a.hkv; h += kThreads) {
+      a.idx.edge_head_base[h] =
+          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch);
+      if (h < a.hkv) a.idx.num_sel[h] = static_cast<int32_t>(head_tot[2 * h + 1]);
+    }
+    if (tid == 0) {
+      // totals: E, work splits, non-empty units (seg_pre holds edges, units, splits)
+      const volatile int64_t* all = seg_pre + 3 * static_cast<int64_t>(nseg);
+      a.idx.totals[0] = all[0];
+      a.idx.totals[1] = all[2];
+      a.idx.totals[2] = all[1];
+    }
+  }
+  const int64_t nbs = a.nbs;
+  const int64_t per_head = nbs + 1;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < a.hkv * per_head;
+       g += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int h = static_cast<int>(g / per_head);
+    const int64_t p = g - h * per_head;
+    if (p >= head_tot[2 * h + 1]) {
+      a.idx.sel_offsets[g] = static_cast<int32_t>(head_tot[2 * h + 0]);
+      if (p < nbs) a.idx.sel_slots[h * nbs + p] = -1;
     }
   }
 }
 
-// sel_offsets[h, p] = head total and sel_slots[h, p] = -1 for p >= num_sel[h].
-__global__ void index_plateau_kernel(int32_t* __restrict__ sel_slots,
-                                     int32_t* __restrict__ sel_offsets,
-                                     const int32_t* __restrict__ num_sel,
-                                     const int64_t* __restrict__ edge_head_base, int64_t nbs) {
-  const int h = blockIdx.y;
-  const int64_t ns_raw = num_sel[h] > 0 ? num_sel[h] : 0;
-  const int64_t ns = ns_raw < nbs + 1 ? ns_raw : nbs + 1;
-  const int32_t total = static_cast<int32_t>(edge_head_base[h + 1] - edge_head_base[h]);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t p = ns + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p <= nbs;
-       p += stride) {
-    sel_offsets[h * (nbs + 1) + p] = total;
-    if (p < nbs) sel_slots[h * nbs + p] = -1;
-  }
+size_t index_smem_bytes(int msb, int batch, int hkv) {
+  return 16 * static_cast<size_t>(hkv) +
+         4 * (3 * static_cast<size_t>(msb > 0 ? msb : 1) + 2 * (static_cast<size_t>(batch) + 1));
 }
 
 }  // namespace
 
-WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch) {
+int64_t index_chunks_per_head(const int64_t* cu_host, int32_t batch, int32_t topk,
+                              int64_t* multi_slots) {
+  int64_t c = 0, m = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t n = (cu_host[b + 1] - cu_host[b]) * topk;
+    const int64_t nc = (n + kChunkEntries - 1) / kChunkEntries;
+    c += nc;
+    if (nc > 1) m += nc;
+  }
+  if (multi_slots) *multi_slots = m;
+  return c;
+}
+
+int64_t index_hist_slot_bound(int64_t tq, int32_t topk) {
+  // Per head: a segment with more than one chunk has n > kChunkEntries entries
+  // and ceil(n / kChunkEntries) < 2 n / kChunkEntries chunks.
+  return 2 * (tq * topk) / kChunkEntries + 1;
+}
+
+WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t hist_slots_per_head,
+                                 int32_t msb) {
   WorkspaceLayout L{};
   const size_t nseg = static_cast<size_t>(hkv) * batch;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  L.ticket = 0;
-  L.seg_a = 256;
-  L.seg_b = up(L.seg_a + 8 * nseg);
-  L.head_units = up(L.seg_b + 8 * nseg);
-  L.zero_bytes = L.head_units;
-  L.total = up(L.head_units + 4 * static_cast<size_t>(hkv));
+  L.barrier = 0;
+  L.seg_done = 256;
+  L.seg_tot = up(L.seg_done + 4 * nseg);
+  L.zero_bytes = L.seg_tot;                       // barrier and per-segment counters
+  L.seg_pre = up(L.seg_tot + 12 * nseg);
+  L.hist = up(L.seg_pre + 24 * (nseg + 1));
+  L.total = up(L.hist + 4 * static_cast<size_t>(hkv) * static_cast<size_t>(hist_slots_per_head) *
+                            static_cast<size_t>(msb > 0 ? msb : 1));
   return L;
 }
 
-cudaError_t launch_build_index(const IndexArgs& a, cudaStream_t stream) {
-  const WorkspaceLayout lay = workspace_layout(a.hkv, a.batch);
+cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
+                               int64_t hist_slots_per_head, cudaStream_t stream) {
+  const WorkspaceLayout lay = workspace_layout(a.hkv, a.batch, hist_slots_per_head, a.msb);
   cudaError_t err = cudaMemsetAsync(a.idx.workspace, 0, lay.zero_bytes, stream);
   if (err != cudaSuccess) return err;
-  err = cudaMemsetAsync(a.idx.totals, 0, 4 * sizeof(int64_t), stream);
-  if (err != cudaSuccess) return err;
-  const size_t smem = 2 * sizeof(int32_t) * static_cast<size_t>(a.msb > 0 ? a.msb : 1);
+  const size_t smem = index_smem_bytes(a.msb, a.batch, a.hkv);
+  if (smem > 227 * 1024) return cudaErrorNotSupported;
   if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(index_segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  const int nseg = a.hkv * a.batch;
-  index_segments_kernel<<<nseg, kThreads, smem, stream>>>(a, lay, nseg);
-  err = cudaGetLastError();
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_kernel, kThreads, smem);
   if (err != cudaSuccess) return err;
-  const int64_t per_head = a.nbs + 1;
-  int gx = static_cast<int>(std::min<int64_t>((per_head + 255) / 256,
-                                              std::max(1, device_sm_count() * 4 / a.hkv + 1)));
-  if (gx < 1) gx = 1;
-  index_plateau_kernel<<<dim3(gx, a.hkv), 256, 0, stream>>>(
-      a.idx.sel_slots, a.idx.sel_offsets, a.idx.num_sel, a.idx.edge_head_base, a.nbs);
-  return cudaGetLastError();
+  if (per_sm < 1) return cudaErrorNotSupported;
+  const int64_t n_chunks = chunks_per_head * a.hkv;
+  int64_t grid = static_cast<int64_t>(per_sm) * device_sm_count();
+  const int64_t plateau_ctas = (static_cast<int64_t>(a.hkv) * (a.nbs + 1) + kThreads - 1) / kThreads;
+  const int64_t want = std::max<int64_t>(std::max<int64_t>(n_chunks, plateau_ctas), 1);
+  if (grid > want) grid = want;
+  IndexArgs args = a;
+  WorkspaceLayout layout = lay;
+  int64_t nch = n_chunks;
+  void* params[] = {&args, &layout, &nch};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(index_kernel),
+                                     dim3(static_cast<unsigned>(grid)), dim3(kThreads), params,
+                                     smem, stream);
 }
 
 }  // namespace sa

@@ -9,17 +9,28 @@
 
 namespace sa {
 
+// Entries of one (kv head, sequence) segment handled by one CTA of the index
+// kernel at a time.
+constexpr int kChunkEntries = 4096;
+
 // Layout of the index workspace (bytes from its start).
 struct WorkspaceLayout {
-  size_t ticket;        // uint32: next segment ticket of the index kernel
-  size_t seg_a;         // uint64[hkv*batch]: flag | edges
-  size_t seg_b;         // uint64[hkv*batch]: flag | units | splits
-  size_t head_units;    // int32[hkv]: non-empty units before head h
+  size_t barrier;       // uint32[2]: grid barrier counter and generation
+  size_t seg_done;      // uint32[hkv*batch]: chunks of the segment that finished phase 1
+  size_t seg_tot;       // int32[hkv*batch][3]: edges, non-empty bins, work splits
+  size_t seg_pre;       // int64[hkv*batch+1][3]: exclusive prefixes of seg_tot
+  size_t hist;          // int32[hkv][slots][msb]: histograms of multi-chunk segments
   size_t zero_bytes;    // bytes cleared at the start of every build
   size_t total;
 };
 
-WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch);
+WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t hist_slots_per_head,
+                                 int32_t msb);
+// Chunks of one head (and, in *multi_slots, chunks of its multi-chunk segments).
+int64_t index_chunks_per_head(const int64_t* cu_host, int32_t batch, int32_t topk,
+                              int64_t* multi_slots);
+// Upper bound of the multi-chunk histogram slots of one head.
+int64_t index_hist_slot_bound(int64_t tq, int32_t topk);
 
 struct IndexArgs {
   const int32_t* selected;
@@ -31,7 +42,8 @@ struct IndexArgs {
   sa_index idx;             // output arrays + workspace
 };
 
-cudaError_t launch_build_index(const IndexArgs& a, cudaStream_t stream);
+cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
+                               int64_t hist_slots_per_head, cudaStream_t stream);
 
 struct ForwardArgs {
   const float* q;

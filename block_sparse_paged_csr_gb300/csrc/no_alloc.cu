@@ -19,8 +19,9 @@
 
 namespace {
 
-// 288 KiB: enough for hkv * batch up to about 18,000 (kv head, sequence)
-// segments.
+// 288 KiB: 40 bytes per (kv head, sequence) segment, plus, for sequences
+// with more than 4096 (query, rank) entries per kv head, msb 4-byte counters
+// per 4096 entries (see workspace_layout in index.cu).
 constexpr size_t kStaticScratchBytes = 288 * 1024;
 
 static __device__ __align__(256) unsigned char g_index_scratch[kStaticScratchBytes];
@@ -56,9 +57,15 @@ extern "C" sa_status sa_build_index_no_alloc(const int32_t* selected, int64_t tq
                                              int32_t block_size, int32_t page_size,
                                              int32_t split_edges, sa_index* idx, void* stream) {
   if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
-  if (hkv > 0 && batch > 0 &&
-      sa::workspace_layout(hkv, batch).total > kStaticScratchBytes)
-    return SA_ERR_UNSUPPORTED;  // more (kv head, sequence) segments than the scratch holds
+  if (hkv > 0 && batch > 0 && topk > 0 && cu_seqlens_q_host != nullptr && block_size > 0 &&
+      page_size > 0 && block_size % page_size == 0) {
+    int64_t multi_slots = 0;
+    sa::index_chunks_per_head(cu_seqlens_q_host, batch, topk, &multi_slots);
+    const int64_t msb = max_pages / (block_size / page_size);
+    if (sa::workspace_layout(hkv, batch, multi_slots, static_cast<int32_t>(msb)).total >
+        kStaticScratchBytes)
+      return SA_ERR_UNSUPPORTED;  // the problem needs more scratch than the array holds
+  }
   void* scratch = nullptr;
   if (hkv > 0 && batch > 0) {
     const sa_status st = scratch_for_current_device(&scratch);

@@ -12,7 +12,7 @@ namespace sa {
 // Upper bounds of spin loops.  A wait that runs out records
 // SA_ERR_DEVICE_TIMEOUT and lets the kernel return instead of hanging.
 constexpr uint32_t kSpinLimit = 1u << 22;        // ~0.25-4 s with backoff
-constexpr int kMaxMsb = 24576;                    // bins of the index kernel
+constexpr int kMaxMsb = 16384;                    // bins of the index kernel (3 per block in shared memory)
 
 // Record the first device-side error of a call in the index status word.
 __device__ __forceinline__ void report(int64_t* status_word, int code) {

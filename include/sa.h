@@ -137,7 +137,7 @@ const char *sa_version(void);
 /*
  * Sizes for an index over selected[tq, hkv, topk] with `batch` sequences and
  * block tables of `max_pages` columns.  Fails with SA_ERR_BLOCK_PAGE,
- * SA_ERR_EMPTY, SA_ERR_UNSUPPORTED (msb above 24576, or tq*hkv*topk >= 2^31)
+ * SA_ERR_EMPTY, SA_ERR_UNSUPPORTED (msb above 16384, or tq*hkv*topk >= 2^31)
  * or SA_ERR_INVALID_ARGUMENT (out == NULL).
  */
 sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t batch,
@@ -183,8 +183,10 @@ sa_status sa_build_index(const int32_t *selected, int64_t tq, int32_t hkv, int32
  * or host runtimes without a device allocator.  The call itself allocates
  * nothing (no cudaMalloc, cudaFree or allocating library routine).
  *
- *   - Returns SA_ERR_UNSUPPORTED when hkv * batch (kv head, sequence)
- *     segments need more scratch than the array holds (about 18,000).
+ *   - Returns SA_ERR_UNSUPPORTED when the problem needs more scratch than
+ *     the array holds: 16 bytes per (kv head, sequence) segment (so at most
+ *     about 18,000 segments), plus, for sequences with more than 4096
+ *     (query, rank) entries per kv head, msb 4-byte counters per 4096 entries.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture on the device.

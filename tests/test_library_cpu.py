@@ -90,7 +90,7 @@ def test_build_index_host_checks(lib):
     assert _build(lib, cu=np.array([1, 4], np.int64)) == names["CU_SEQLENS"]
     assert _build(lib, cu=np.array([0, 3, 2, 4], np.int64), batch=3) == names["CU_SEQLENS"]
     assert _build(lib, cu=np.array([0, 3], np.int64)) == names["SHAPE"]
-    assert _build(lib, max_pages=2 * 24577) == names["UNSUPPORTED"]
+    assert _build(lib, max_pages=2 * 16385) == names["UNSUPPORTED"]
     # everything valid but no device arrays: rejected before any launch
     assert _build(lib) == names["INVALID_ARGUMENT"]
 
