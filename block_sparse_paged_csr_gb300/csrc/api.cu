@@ -180,10 +180,13 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   if (num_pages < 0) return SA_ERR_SHAPE;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
-  if (path == SA_PATH_TENSOR_CORE) return SA_ERR_UNSUPPORTED;
-  if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL)
+  if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
+      path != SA_PATH_TENSOR_CORE)
     return SA_ERR_INVALID_ARGUMENT;
-  if (!sa::forward_cc_supported(head_dim, block_size, kv_bf16)) return SA_ERR_UNSUPPORTED;
+  const bool tc_ok = sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv);
+  if (path == SA_PATH_TENSOR_CORE && !tc_ok) return SA_ERR_UNSUPPORTED;
+  if (path != SA_PATH_TENSOR_CORE && !sa::forward_cc_supported(head_dim, block_size, kv_bf16))
+    return SA_ERR_UNSUPPORTED;
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
       !l_partial)
     return SA_ERR_INVALID_ARGUMENT;
@@ -212,6 +215,9 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   a.scale = softmax_scale;
   a.causal = causal != 0;
   a.sel_slots = idx->sel_slots;
+  a.sel_offsets = idx->sel_offsets;
+  a.num_sel = idx->num_sel;
+  a.edge_head_base = idx->edge_head_base;
   a.edges = idx->edges;
   a.splits = idx->splits;
   a.totals = idx->totals;
@@ -221,14 +227,19 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   a.l_partial = l_partial;
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
   // Decode-shaped problems (about one query per sequence, so few rows per
-  // work split) go to the pipelined kernel; the general kernel takes the rest.
+  // work split) go to the pipelined CUDA-core kernel; problems whose units
+  // gather many rows go to the tensor cores; the general kernel takes the rest.
   const bool dec_ok =
       sa::forward_dec_supported(head_dim, block_size, page_size, a.qhead, kv_bf16);
   const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
-  const bool use_dec = dec_ok && (path == SA_PATH_CUDA_CORE ||
-                                  (path == SA_PATH_AUTO && decode_like));
-  const cudaError_t err = use_dec ? sa::launch_forward_dec(a, static_cast<cudaStream_t>(stream))
-                                  : sa::launch_forward_cc(a, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (path == SA_PATH_TENSOR_CORE || (path == SA_PATH_AUTO && !decode_like && tc_ok))
+    err = sa::launch_forward_tc(a, s);
+  else if (dec_ok && (path == SA_PATH_CUDA_CORE || (path == SA_PATH_AUTO && decode_like)))
+    err = sa::launch_forward_dec(a, s);
+  else
+    err = sa::launch_forward_cc(a, s);
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
@@ -271,7 +282,9 @@ sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return SA_ERR_BLOCK_PAGE;
-  if (!sa::forward_cc_supported(head_dim, block_size, kv_dtype == SA_DTYPE_BF16))
+  if (!sa::forward_cc_supported(head_dim, block_size, kv_dtype == SA_DTYPE_BF16) &&
+      !(path == SA_PATH_TENSOR_CORE &&
+        sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv)))
     return SA_ERR_UNSUPPORTED;
   sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q, batch,
                                 used_kv_lens, max_pages, block_size, page_size, split_edges, idx,

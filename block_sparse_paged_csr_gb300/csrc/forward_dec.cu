@@ -419,6 +419,9 @@ cudaError_t launch_dec(const ForwardArgs& a, cudaStream_t stream) {
   cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (err != cudaSuccess) return err;
   int64_t grid = device_sm_count();
   const int64_t need = (a.max_splits + WARPS - 1) / WARPS;
   if (grid > need) grid = need;

@@ -60,6 +60,9 @@ struct ForwardArgs {
   int causal;
   // index
   const int32_t* sel_slots;
+  const int32_t* sel_offsets;
+  const int32_t* num_sel;
+  const int64_t* edge_head_base;
   const int32_t* edges;
   const int32_t* splits;
   int64_t* totals;          // [0] E, [1] splits, [3] status
@@ -73,6 +76,10 @@ struct ForwardArgs {
 // Returns cudaErrorNotSupported when the shape has no kernel.
 cudaError_t launch_forward_cc(const ForwardArgs& a, cudaStream_t stream);
 bool forward_cc_supported(int head_dim, int block_size, int kv_bf16);
+
+// Tensor-core (tcgen05) forward for units with many gathered rows.
+cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t stream);
+bool forward_tc_supported(int head_dim, int block_size, int page_size, int qhead);
 
 // Pipelined decode-shaped forward (head_dim 128, few rows per split).
 cudaError_t launch_forward_dec(const ForwardArgs& a, cudaStream_t stream);

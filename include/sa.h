@@ -66,7 +66,9 @@ typedef enum sa_path {
   SA_PATH_AUTO = 0,              /* pick per problem shape                          */
   SA_PATH_CUDA_CORE = 1,         /* f32 FMA kernels: the pipelined decode kernel
                                     where its shape limits allow, else the general one */
-  SA_PATH_TENSOR_CORE = 2,       /* tcgen05 kernel; SA_ERR_UNSUPPORTED where absent */
+  SA_PATH_TENSOR_CORE = 2,       /* tcgen05 kernel (head_dim 128, block 64 or 128,
+                                    qhead dividing 128; bf16 operands, f32
+                                    accumulation); SA_ERR_UNSUPPORTED elsewhere     */
   SA_PATH_CUDA_CORE_GENERAL = 3  /* the general f32 FMA kernel only                 */
 } sa_path;
 
@@ -226,7 +228,10 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * live key holds (o = 0, m = -inf, l = 0).  Only the first E*qhead rows are
  * written.  Supported: head_dim a multiple of 4 (f32) or 8 (bf16), at most
  * 256, and block_size * head_dim * elt * 2 <= 160 KiB; otherwise
- * SA_ERR_UNSUPPORTED.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * SA_ERR_UNSUPPORTED.  SA_PATH_AUTO sends decode-shaped problems (tq at most
+ * twice the batch) to the pipelined CUDA-core kernel and the others to the
+ * tensor cores where supported (operands rounded to bf16; use
+ * SA_PATH_CUDA_CORE for f32 arithmetic throughout).  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
  * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
  */
 sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,

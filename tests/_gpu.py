@@ -9,7 +9,20 @@ import block_sparse_paged_csr_gb300 as sa
 import inputs
 
 TOL_F32 = 1e-4      # f32 arithmetic on the CUDA-core path (row-normalised)
-TOL_TC = 2e-2       # tensor-core path (bf16 / tf32 operands)
+TOL_TC = 2e-2       # tensor-core path (bf16 operands)
+
+
+def auto_uses_tensor_cores(w) -> bool:
+    """Mirror of the library's SA_PATH_AUTO rule: problems that are not
+    decode-shaped go to the tensor cores where that kernel supports them."""
+    decode_like = w.tq <= 2 * w.batch
+    tc_ok = (w.head_dim == 128 and w.block_size in (64, 128) and w.block_size % w.page_size == 0
+             and 128 % w.qhead == 0)
+    return (not decode_like) and tc_ok
+
+
+def auto_tol(w) -> float:
+    return TOL_TC if auto_uses_tensor_cores(w) else TOL_F32
 
 
 def device_workload(w: inputs.Workload, dev="cuda", fill_on_device=False):
