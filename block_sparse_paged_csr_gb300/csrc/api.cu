@@ -184,7 +184,11 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
       path != SA_PATH_TENSOR_CORE)
     return SA_ERR_INVALID_ARGUMENT;
   const bool tc_ok = sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv);
-  if (path == SA_PATH_TENSOR_CORE && !tc_ok) return SA_ERR_UNSUPPORTED;
+  const bool mma_ok =
+      sa::forward_dec_mma_supported(head_dim, block_size, page_size, hq / hkv, kv_bf16);
+  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
+  if (path == SA_PATH_TENSOR_CORE && !(decode_like ? (mma_ok || tc_ok) : tc_ok))
+    return SA_ERR_UNSUPPORTED;
   if (path != SA_PATH_TENSOR_CORE && !sa::forward_cc_supported(head_dim, block_size, kv_bf16))
     return SA_ERR_UNSUPPORTED;
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
@@ -231,10 +235,13 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   // gather many rows go to the tensor cores; the general kernel takes the rest.
   const bool dec_ok =
       sa::forward_dec_supported(head_dim, block_size, page_size, a.qhead, kv_bf16);
-  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (path == SA_PATH_TENSOR_CORE || (path == SA_PATH_AUTO && !decode_like && tc_ok))
+  // bf16 decode: warp-level MMA (AUTO and TENSOR_CORE); other tensor-core
+  // work: tcgen05.
+  if (decode_like && mma_ok && (path == SA_PATH_AUTO || path == SA_PATH_TENSOR_CORE))
+    err = sa::launch_forward_dec_mma(a, s);
+  else if (path == SA_PATH_TENSOR_CORE || (path == SA_PATH_AUTO && !decode_like && tc_ok))
     err = sa::launch_forward_tc(a, s);
   else if (dec_ok && (path == SA_PATH_CUDA_CORE || (path == SA_PATH_AUTO && decode_like)))
     err = sa::launch_forward_dec(a, s);

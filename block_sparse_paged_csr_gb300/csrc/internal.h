@@ -81,6 +81,11 @@ bool forward_cc_supported(int head_dim, int block_size, int kv_bf16);
 cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t stream);
 bool forward_tc_supported(int head_dim, int block_size, int page_size, int qhead);
 
+// Decode-shaped forward with bf16 K/V on warp-level tensor-core MMA.
+cudaError_t launch_forward_dec_mma(const ForwardArgs& a, cudaStream_t stream);
+bool forward_dec_mma_supported(int head_dim, int block_size, int page_size, int qhead,
+                               int kv_bf16);
+
 // Pipelined decode-shaped forward (head_dim 128, few rows per split).
 cudaError_t launch_forward_dec(const ForwardArgs& a, cudaStream_t stream);
 bool forward_dec_supported(int head_dim, int block_size, int page_size, int qhead, int kv_bf16);

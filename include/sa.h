@@ -66,9 +66,12 @@ typedef enum sa_path {
   SA_PATH_AUTO = 0,              /* pick per problem shape                          */
   SA_PATH_CUDA_CORE = 1,         /* f32 FMA kernels: the pipelined decode kernel
                                     where its shape limits allow, else the general one */
-  SA_PATH_TENSOR_CORE = 2,       /* tcgen05 kernel (head_dim 128, block 64 or 128,
-                                    qhead dividing 128; bf16 operands, f32
-                                    accumulation); SA_ERR_UNSUPPORTED elsewhere     */
+  SA_PATH_TENSOR_CORE = 2,       /* tensor cores, head_dim 128: decode-shaped
+                                    problems with bf16 K/V use warp-level MMA (Q and
+                                    P split into two bf16 parts); others use the
+                                    tcgen05 kernel (block 64 or 128, qhead dividing
+                                    128, bf16 operands); f32 accumulation;
+                                    SA_ERR_UNSUPPORTED elsewhere                   */
   SA_PATH_CUDA_CORE_GENERAL = 3  /* the general f32 FMA kernel only                 */
 } sa_path;
 
@@ -229,9 +232,10 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * written.  Supported: head_dim a multiple of 4 (f32) or 8 (bf16), at most
  * 256, and block_size * head_dim * elt * 2 <= 160 KiB; otherwise
  * SA_ERR_UNSUPPORTED.  SA_PATH_AUTO sends decode-shaped problems (tq at most
- * twice the batch) to the pipelined CUDA-core kernel and the others to the
- * tensor cores where supported (operands rounded to bf16; use
- * SA_PATH_CUDA_CORE for f32 arithmetic throughout).  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * twice the batch) to the pipelined CUDA-core kernel (f32 K/V) or to the
+ * warp-level MMA kernel (bf16 K/V), and the others to the tcgen05 kernel
+ * where supported (operands rounded to bf16; use SA_PATH_CUDA_CORE for f32
+ * arithmetic throughout).  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
  * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
  */
 sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,

@@ -258,3 +258,16 @@ def test_tensor_core_shapes(bs, ps, qhead, dt, causal):
     w.causal = causal
     w.block_tables[1, 2] = -1              # a hole inside a live block
     _check_against_oracle(w, _gpu.device_workload(w), 7, sa.PATH_TENSOR_CORE, _gpu.TOL_TC)
+
+
+@pytest.mark.parametrize("bs,ps,qhead", [(64, 16, 8), (32, 16, 1), (128, 64, 4), (64, 8, 2),
+                                         (128, 16, 16), (64, 32, 8)])
+def test_decode_mma_shapes(bs, ps, qhead):
+    """bf16 decode on warp-level MMA (split bf16 operands): f32-class
+    accuracy, including repeated blocks (multi-edge units -> row groups)."""
+    w = inputs.gqa_decode(seed=3 * bs + ps + qhead, batch=7, kv_min=900, kv_max=2100, hkv=2,
+                          hq=2 * qhead, head_dim=128, page_size=ps, block_size=bs, topk=6,
+                          kv_dtype="bf16")
+    w.block_tables[2, 1] = -1
+    w.selected[3, 1, 2] = w.selected[3, 1, 1]      # a block selected at two ranks
+    _check_against_oracle(w, _gpu.device_workload(w), 0, sa.PATH_TENSOR_CORE, _gpu.TOL_F32)
