@@ -358,9 +358,9 @@ def run_ours(args, rank, world, local_rank):
     fwd_gbs = acct["forward"] / (fwd_ms / 1e3) / 1e9
     step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
-    decode_like = w.tq <= 2 * w.batch and w.head_dim == 128
-    fwd_file = "forward_dec.cu" if decode_like else "forward_cc.cu"
-    fwd_kernel = "forward_dec_kernel" if decode_like else "forward_cc_kernel"
+    fwd_kernel = sa.sa_forward_kernel_name(w.tq, w.batch, w.hkv, w.hq, w.head_dim, w.block_size,
+                                           w.page_size, w.kv_dtype, sa.PATH_AUTO)
+    fwd_file = fwd_kernel.replace("_kernel", ".cu")
     traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", ""))
     value = world * w.tq * args.steps / elapsed_s
     dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"

@@ -27,7 +27,7 @@ from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_CUD
                       PATH_TENSOR_CORE, STATUS_NAMES)
 
 __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
-           "sa_build_index_no_alloc", "sa_forward",
+           "sa_build_index_no_alloc", "sa_forward", "sa_forward_kernel_name",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
            "PATH_CUDA_CORE_GENERAL"]
@@ -222,6 +222,18 @@ def _kv_dtype(k):
     if k.dtype == torch.bfloat16:
         return DTYPE_BF16
     raise TypeError(f"k_pages/v_pages must be float32 or bfloat16, got {k.dtype}")
+
+
+def sa_forward_kernel_name(tq, batch, hkv, hq, head_dim, block_size, page_size, kv_dtype="f32",
+                           path=PATH_AUTO):
+    """Name of the kernel sa_forward launches for this problem shape, or None
+    where sa_forward would refuse it.  Host only."""
+    c = _native.SaIndex()
+    c.tq, c.batch, c.hkv = int(tq), int(batch), int(hkv)
+    dt = {"f32": DTYPE_F32, "bf16": DTYPE_BF16}[kv_dtype]
+    name = _native.load().sa_forward_kernel_name(ctypes.byref(c), hq, head_dim, block_size,
+                                                 page_size, dt, int(path))
+    return None if name is None else name.decode()
 
 
 def partial_rows(index: Index, hq: int) -> int:

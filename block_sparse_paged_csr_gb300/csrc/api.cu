@@ -29,6 +29,41 @@ namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+enum class FwdKernel { kNone, kGeneral, kDecode, kDecodeMma, kTensor };
+
+// The forward kernel a call takes.  Decode-shaped problems (tq at most twice
+// the batch: about one query per sequence, so few rows per work split) go to
+// the per-warp decode kernels (warp-level MMA for bf16 K/V, f32 FMA
+// otherwise); problems whose units gather many rows go to the tcgen05
+// kernel; the general f32 kernel takes whatever the others do not support.
+FwdKernel choose_forward(const sa_index* idx, int32_t qhead, int32_t head_dim,
+                         int32_t block_size, int32_t page_size, int kv_bf16, sa_path path) {
+  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
+  const bool tc_ok = sa::forward_tc_supported(head_dim, block_size, page_size, qhead);
+  const bool mma_ok =
+      sa::forward_dec_mma_supported(head_dim, block_size, page_size, qhead, kv_bf16);
+  const bool dec_ok = sa::forward_dec_supported(head_dim, block_size, page_size, qhead, kv_bf16);
+  const bool cc_ok = sa::forward_cc_supported(head_dim, block_size, kv_bf16);
+  switch (path) {
+    case SA_PATH_TENSOR_CORE:
+      if (decode_like && mma_ok) return FwdKernel::kDecodeMma;
+      return tc_ok ? FwdKernel::kTensor : FwdKernel::kNone;
+    case SA_PATH_CUDA_CORE:
+      if (!cc_ok) return FwdKernel::kNone;
+      return dec_ok ? FwdKernel::kDecode : FwdKernel::kGeneral;
+    case SA_PATH_CUDA_CORE_GENERAL:
+      return cc_ok ? FwdKernel::kGeneral : FwdKernel::kNone;
+    case SA_PATH_AUTO:
+      if (!cc_ok) return FwdKernel::kNone;
+      if (decode_like && mma_ok) return FwdKernel::kDecodeMma;
+      if (decode_like && dec_ok) return FwdKernel::kDecode;
+      if (!decode_like && tc_ok) return FwdKernel::kTensor;
+      return FwdKernel::kGeneral;
+    default:
+      return FwdKernel::kNone;
+  }
+}
+
 sa_status validate_cu_host(const int64_t* cu, int32_t batch) {
   if (cu == nullptr || batch < 1 || cu[0] != 0) return SA_ERR_CU_SEQLENS;
   for (int32_t b = 1; b <= batch; ++b)
@@ -183,14 +218,9 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
       path != SA_PATH_TENSOR_CORE)
     return SA_ERR_INVALID_ARGUMENT;
-  const bool tc_ok = sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv);
-  const bool mma_ok =
-      sa::forward_dec_mma_supported(head_dim, block_size, page_size, hq / hkv, kv_bf16);
-  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
-  if (path == SA_PATH_TENSOR_CORE && !(decode_like ? (mma_ok || tc_ok) : tc_ok))
-    return SA_ERR_UNSUPPORTED;
-  if (path != SA_PATH_TENSOR_CORE && !sa::forward_cc_supported(head_dim, block_size, kv_bf16))
-    return SA_ERR_UNSUPPORTED;
+  const FwdKernel kernel =
+      choose_forward(idx, hq / hkv, head_dim, block_size, page_size, kv_bf16, path);
+  if (kernel == FwdKernel::kNone) return SA_ERR_UNSUPPORTED;
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
       !l_partial)
     return SA_ERR_INVALID_ARGUMENT;
@@ -230,25 +260,33 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   a.m_partial = m_partial;
   a.l_partial = l_partial;
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
-  // Decode-shaped problems (about one query per sequence, so few rows per
-  // work split) go to the pipelined CUDA-core kernel; problems whose units
-  // gather many rows go to the tensor cores; the general kernel takes the rest.
-  const bool dec_ok =
-      sa::forward_dec_supported(head_dim, block_size, page_size, a.qhead, kv_bf16);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  // bf16 decode: warp-level MMA (AUTO and TENSOR_CORE); other tensor-core
-  // work: tcgen05.
-  if (decode_like && mma_ok && (path == SA_PATH_AUTO || path == SA_PATH_TENSOR_CORE))
-    err = sa::launch_forward_dec_mma(a, s);
-  else if (path == SA_PATH_TENSOR_CORE || (path == SA_PATH_AUTO && !decode_like && tc_ok))
-    err = sa::launch_forward_tc(a, s);
-  else if (dec_ok && (path == SA_PATH_CUDA_CORE || (path == SA_PATH_AUTO && decode_like)))
-    err = sa::launch_forward_dec(a, s);
-  else
-    err = sa::launch_forward_cc(a, s);
+  switch (kernel) {
+    case FwdKernel::kDecodeMma: err = sa::launch_forward_dec_mma(a, s); break;
+    case FwdKernel::kTensor: err = sa::launch_forward_tc(a, s); break;
+    case FwdKernel::kDecode: err = sa::launch_forward_dec(a, s); break;
+    default: err = sa::launch_forward_cc(a, s); break;
+  }
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+const char* sa_forward_kernel_name(const sa_index* idx, int32_t hq, int32_t head_dim,
+                                   int32_t block_size, int32_t page_size, sa_dtype kv_dtype,
+                                   sa_path path) {
+  if (idx == nullptr || idx->hkv <= 0 || hq <= 0 || hq % idx->hkv != 0) return nullptr;
+  if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
+    return nullptr;
+  if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return nullptr;
+  switch (choose_forward(idx, hq / idx->hkv, head_dim, block_size, page_size,
+                         kv_dtype == SA_DTYPE_BF16 ? 1 : 0, path)) {
+    case FwdKernel::kDecodeMma: return "forward_dec_mma_kernel";
+    case FwdKernel::kTensor: return "forward_tc_kernel";
+    case FwdKernel::kDecode: return "forward_dec_kernel";
+    case FwdKernel::kGeneral: return "forward_cc_kernel";
+    default: return nullptr;
+  }
 }
 
 sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m_partial,

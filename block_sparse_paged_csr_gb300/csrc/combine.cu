@@ -2,8 +2,8 @@
 // module doc of forward.rs (alice-llm sparse_attention).  One warp per
 // (query, q-head): lanes gather the row's partial positions through inv and
 // reduce M = max m_r and L = sum exp(m_r - M) l_r; then the live partials are
-// visited one by one (ballot order) and each lane accumulates four or eight of
-// the head_dim outputs with 16-byte loads.
+// visited in ballot order, eight rows loaded at a time, and each lane
+// accumulates four or eight of the head_dim outputs with 16-byte loads.
 #include <cstdint>
 
 #include "internal.h"
@@ -60,23 +60,38 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
         }
       }
       unsigned live = __ballot_sync(0xffffffffu, wgt > 0.f);
+      // Up to kBatch partial rows are loaded before any is used, so their
+      // latencies overlap.
+      constexpr int kBatch = 8;
       while (live) {
-        const int src = __ffs(live) - 1;
-        live &= live - 1;
-        const float wv = __shfl_sync(0xffffffffu, wgt, src);
-        const int64_t pr = __shfl_sync(0xffffffffu, prow, src);
-        const float4* orow = reinterpret_cast<const float4*>(a.o_partial + pr * d);
+        float wv[kBatch];
+        float4 v[kBatch][kChunks];
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          const int ch = lane + 32 * c;
-          if (ch < nc) {
-            const float4 v = orow[ch];
-            acc[c].x = fmaf(wv, v.x, acc[c].x);
-            acc[c].y = fmaf(wv, v.y, acc[c].y);
-            acc[c].z = fmaf(wv, v.z, acc[c].z);
-            acc[c].w = fmaf(wv, v.w, acc[c].w);
+        for (int t = 0; t < kBatch; ++t) {
+          wv[t] = 0.f;
+          int64_t pr = 0;
+          if (live) {
+            const int src = __ffs(live) - 1;
+            live &= live - 1;
+            wv[t] = __shfl_sync(0xffffffffu, wgt, src);
+            pr = __shfl_sync(0xffffffffu, prow, src);
+          }
+          const float4* orow = reinterpret_cast<const float4*>(a.o_partial + pr * d);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const int ch = lane + 32 * c;
+            v[t][c] = (wv[t] > 0.f && ch < nc) ? orow[ch] : make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
+#pragma unroll
+        for (int t = 0; t < kBatch; ++t)
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            acc[c].x = fmaf(wv[t], v[t][c].x, acc[c].x);
+            acc[c].y = fmaf(wv[t], v[t][c].y, acc[c].y);
+            acc[c].z = fmaf(wv[t], v[t][c].z, acc[c].z);
+            acc[c].w = fmaf(wv[t], v[t][c].w, acc[c].w);
+          }
       }
     }
 #pragma unroll

@@ -247,6 +247,19 @@ sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
                      void *stream);
 
 /*
+ * Name of the kernel sa_forward would launch for these arguments and `path`
+ * ("forward_dec_mma_kernel", "forward_tc_kernel", "forward_dec_kernel" or
+ * "forward_cc_kernel"), or NULL where sa_forward would refuse them (bad head
+ * counts or block/page sizes, or SA_ERR_UNSUPPORTED).  Host only: reads the
+ * geometry fields of idx (hkv, tq, batch), touches no device memory.  The
+ * pages have no counterpart; it lets a caller (or a profiler script) know which
+ * kernel serves a problem shape.  The returned string is static.
+ */
+const char *sa_forward_kernel_name(const sa_index *idx, int32_t hq, int32_t head_dim,
+                                   int32_t block_size, int32_t page_size, sa_dtype kv_dtype,
+                                   sa_path path);
+
+/*
  * Step 3: log-sum-exp combine (forward.rs module doc: "standard FlashAttention
  * log-sum-exp update").  For query i and q-head hq (h = hq / qhead), over
  * ranks r with inv[h, i, r] >= 0: M = max m_r, L = sum exp(m_r - M) l_r,

@@ -13,12 +13,10 @@ TOL_TC = 2e-2       # tensor-core path (bf16 operands)
 
 
 def auto_uses_tensor_cores(w) -> bool:
-    """Mirror of the library's SA_PATH_AUTO rule: problems that are not
-    decode-shaped go to the tensor cores where that kernel supports them."""
-    decode_like = w.tq <= 2 * w.batch
-    tc_ok = (w.head_dim == 128 and w.block_size in (64, 128) and w.block_size % w.page_size == 0
-             and 128 % w.qhead == 0)
-    return (not decode_like) and tc_ok
+    """Whether SA_PATH_AUTO sends this workload to the tcgen05 kernel (bf16
+    operands), as the library itself reports it."""
+    return sa.sa_forward_kernel_name(w.tq, w.batch, w.hkv, w.hq, w.head_dim, w.block_size,
+                                     w.page_size, w.kv_dtype) == "forward_tc_kernel"
 
 
 def auto_tol(w) -> float:

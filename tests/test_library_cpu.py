@@ -120,3 +120,39 @@ def test_forward_and_combine_host_checks(lib):
         names["HEAD_COUNT"]
     assert lib.sa_combine(ctypes.byref(idx), None, None, None, 4, 30, None, None, None) == \
         names["UNSUPPORTED"]
+
+
+def test_forward_kernel_choice(lib):
+    """The kernel each serving workload takes under SA_PATH_AUTO and under
+    each forced path, and refusals where sa_forward would refuse."""
+    import block_sparse_paged_csr_gb300 as sa
+    import inputs
+
+    name = sa.sa_forward_kernel_name
+    auto = {}
+    for wname, builder in inputs.FULL.items():
+        w = builder()
+        auto[wname] = name(w.tq, w.batch, w.hkv, w.hq, w.head_dim, w.block_size, w.page_size,
+                           w.kv_dtype)
+    assert auto["gqa_decode"] == "forward_dec_kernel"
+    assert auto["long_decode"] == "forward_dec_mma_kernel"
+    assert auto["chunked_prefill"] == "forward_tc_kernel"
+    assert auto["chunked_prefill_bf16"] == "forward_tc_kernel"
+    assert auto["skewed"] == "forward_tc_kernel"
+    assert auto["tiny"] == "forward_cc_kernel"      # head_dim 32
+    # forced paths on a decode shape (64 sequences, one query each)
+    geo = (64, 64, 8, 32, 128, 64, 16)
+    assert name(*geo, "f32", sa.PATH_CUDA_CORE) == "forward_dec_kernel"
+    assert name(*geo, "bf16", sa.PATH_CUDA_CORE) == "forward_dec_kernel"
+    assert name(*geo, "f32", sa.PATH_CUDA_CORE_GENERAL) == "forward_cc_kernel"
+    assert name(*geo, "f32", sa.PATH_TENSOR_CORE) == "forward_tc_kernel"
+    assert name(*geo, "bf16", sa.PATH_TENSOR_CORE) == "forward_dec_mma_kernel"
+    # block 16 is below the decode kernels' two 16-key chunks per block
+    assert name(64, 64, 8, 32, 128, 16, 16, "bf16") == "forward_cc_kernel"
+    # tensor cores need head_dim 128
+    assert name(8192, 4, 8, 64, 64, 128, 64, "f32", sa.PATH_TENSOR_CORE) is None
+    assert name(8192, 4, 8, 64, 64, 128, 64, "f32") == "forward_cc_kernel"
+    # refusals: head counts, block/page, head_dim beyond the general kernel
+    assert name(4, 1, 3, 4, 32, 32, 16) is None
+    assert name(4, 1, 2, 4, 32, 32, 24) is None
+    assert name(4, 1, 2, 4, 512, 32, 16) is None
