@@ -76,11 +76,13 @@ def make_workload(name: str, seed: int):
 # --------------------------------------------------------------------------- accounting
 
 
-def algorithmic_bytes(w) -> dict:
+def algorithmic_bytes(w, fused=False) -> dict:
     """Bytes the KV-outer method must move, from the workload's own index
     inputs: each kept (kv head, block) loads its live keys' K and V once, Q is
     read once, the partials are written by the forward and read by the
-    combine, the output is written once."""
+    combine, the output is written once.  On the fused decode path the
+    partials stay on chip, so its one kernel ("forward") moves K, V, Q, the
+    index's inv rows and the output."""
     elt = 2 if w.kv_dtype == "bf16" else 4
     cu = w.cu_seqlens_q
     kv_keys = 0
@@ -110,6 +112,10 @@ def algorithmic_bytes(w) -> dict:
     parts = edges * w.qhead * (w.head_dim + 2) * 4
     out = w.tq * w.hq * w.head_dim * 4
     inv = w.hkv * w.tq * w.topk * 4
+    if fused:
+        return {"kv": kv, "q": q, "partials_write": 0, "partials_read": 0, "out": out,
+                "inv": inv, "edges": edges, "flops": flops,
+                "forward": kv + q + out + inv, "combine": 0, "step": kv + q + out + inv}
     return {"kv": kv, "q": q, "partials_write": parts, "partials_read": parts, "out": out,
             "inv": inv, "edges": edges, "flops": flops,
             "forward": kv + q + parts, "combine": parts + inv + out,
@@ -222,7 +228,10 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     w = make_workload(args.workload, args.seed + rank)
     split = SPLIT_EDGES.get(args.workload.replace("_ncu", ""), 0)
-    acct = algorithmic_bytes(w)
+    fwd_kernel = sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq,
+                                             w.head_dim, w.block_size, w.page_size, w.kv_dtype)
+    fused = fwd_kernel == "fused_dec_kernel"
+    acct = algorithmic_bytes(w, fused)
 
     q, k, v = inputs.device_tensors(w, dev)
     sel = torch.from_numpy(w.selected).to(dev)
@@ -278,6 +287,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {sa.sa_status_string(status)}")
 
     # ---- per-stage durations (same launches, events between the stages) -----
+    # On the fused decode path steps 2 and 3 are one kernel (sa_forward_combine).
     n_stage = min(args.steps, 200)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_stage)]
     o_p, m_p, l_p = partials
@@ -288,10 +298,16 @@ def run_ours(args, rank, world, local_rank):
         sa.sa_build_index(sel, cu_host, cu, used, w.max_pages, w.block_size, w.page_size,
                           split_edges=split, index=index)
         e[1].record(stream)
-        sa.sa_forward(q, k, v, index, bt, cu, used, w.hq, w.hkv, w.head_dim, w.block_size,
-                      w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p)
-        e[2].record(stream)
-        sa.sa_combine(index, o_p, m_p, l_p, w.hq, w.head_dim, out, lse)
+        if fused:
+            sa.sa_forward_combine(q, k, v, index, sel, cu_host, cu, used, bt, w.hq, w.head_dim,
+                                  w.block_size, w.page_size, w.softmax_scale, w.causal,
+                                  split_edges=split, partials=partials, out=out, lse=lse)
+            e[2].record(stream)
+        else:
+            sa.sa_forward(q, k, v, index, bt, cu, used, w.hq, w.hkv, w.head_dim, w.block_size,
+                          w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p)
+            e[2].record(stream)
+            sa.sa_combine(index, o_p, m_p, l_p, w.hq, w.head_dim, out, lse)
         e[3].record(stream)
     torch.cuda.synchronize(dev)
     st = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])
@@ -358,8 +374,6 @@ def run_ours(args, rank, world, local_rank):
     fwd_gbs = acct["forward"] / (fwd_ms / 1e3) / 1e9
     step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
-    fwd_kernel = sa.sa_forward_kernel_name(w.tq, w.batch, w.hkv, w.hq, w.head_dim, w.block_size,
-                                           w.page_size, w.kv_dtype, sa.PATH_AUTO)
     fwd_file = fwd_kernel.replace("_kernel", ".cu")
     traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", ""))
     value = world * w.tq * args.steps / elapsed_s
@@ -379,8 +393,10 @@ def run_ours(args, rank, world, local_rank):
         "step_algorithmic_gbs": step_gbs,
         "step_frac_of_hbm": step_gbs / peak,
         "tflops": acct["flops"] / (ms_per_step / 1e3) / 1e12,
-        "stages_ms": {"index": index_ms, "forward": fwd_ms, "combine": comb_ms},
-        "roofline": {"kernel": f"{fwd_kernel} (sa_forward)", "bound": "hbm",
+        "stages_ms": ({"index": index_ms, "forward_combine": fwd_ms} if fused else
+                      {"index": index_ms, "forward": fwd_ms, "combine": comb_ms}),
+        "roofline": {"kernel": f"{fwd_kernel} ({'sa_forward_combine' if fused else 'sa_forward'})",
+                     "bound": "hbm",
                      "achieved": fwd_gbs, "peak": peak, "unit": "GB/s",
                      "frac": fwd_gbs / peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": acct["forward"],
@@ -389,7 +405,9 @@ def run_ours(args, rank, world, local_rank):
                                                        "step", "forward", "combine")},
         "edges": acct["edges"],
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        # library kernels per step: the index kernel, then the fused decode
+        # kernel or forward + combine
+        "gpu_launches": (2 if fused else 3) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
         "cpu_baseline": (cpu_baseline(w, args)

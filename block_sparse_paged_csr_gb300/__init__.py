@@ -12,6 +12,8 @@ The three steps (crate alice-llm 2.0.0, module sparse_attention):
 * :func:`sa_forward` - per-edge partials o, m, l (``forward.rs``,
   kvouter_forward);
 * :func:`sa_combine` - log-sum-exp merge per (query, q-head);
+* :func:`sa_forward_combine` - steps 2 and 3 on a built index (one fused
+  kernel for batches of one query per sequence);
 * :func:`sa_attention` - the three on one stream without a host sync.
 """
 from __future__ import annotations
@@ -24,10 +26,11 @@ import torch
 
 from . import _native
 from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_CUDA_CORE_GENERAL,
-                      PATH_TENSOR_CORE, STATUS_NAMES)
+                      PATH_FUSED_DECODE, PATH_TENSOR_CORE, STATUS_NAMES)
 
 __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
-           "sa_build_index_no_alloc", "sa_forward", "sa_forward_kernel_name",
+           "sa_build_index_no_alloc", "sa_forward", "sa_forward_combine", "sa_forward_kernel_name",
+           "sa_attention_kernel_name", "PATH_FUSED_DECODE",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
            "PATH_CUDA_CORE_GENERAL"]
@@ -228,11 +231,21 @@ def sa_forward_kernel_name(tq, batch, hkv, hq, head_dim, block_size, page_size, 
                            path=PATH_AUTO):
     """Name of the kernel sa_forward launches for this problem shape, or None
     where sa_forward would refuse it.  Host only."""
-    c = _native.SaIndex()
-    c.tq, c.batch, c.hkv = int(tq), int(batch), int(hkv)
     dt = {"f32": DTYPE_F32, "bf16": DTYPE_BF16}[kv_dtype]
-    name = _native.load().sa_forward_kernel_name(ctypes.byref(c), hq, head_dim, block_size,
-                                                 page_size, dt, int(path))
+    name = _native.load().sa_forward_kernel_name(int(tq), int(batch), hq, hkv, head_dim,
+                                                 block_size, page_size, dt, int(path))
+    return None if name is None else name.decode()
+
+
+def sa_attention_kernel_name(cu_seqlens_q_host, num_pages, hkv, hq, head_dim, block_size,
+                             page_size, kv_dtype="f32", path=PATH_AUTO):
+    """The kernel sa_attention runs for steps 2 and 3 ("fused_dec_kernel" on
+    the fused decode path), or None where it would refuse the shape."""
+    cu = _host_i64(cu_seqlens_q_host)
+    dt = {"f32": DTYPE_F32, "bf16": DTYPE_BF16}[kv_dtype]
+    name = _native.load().sa_attention_kernel_name(
+        int(cu[-1]), len(cu) - 1, cu.ctypes.data, int(num_pages), hq, hkv, head_dim, block_size,
+        page_size, dt, int(path))
     return None if name is None else name.decode()
 
 
@@ -286,6 +299,39 @@ def sa_combine(index: Index, o_partial, m_partial, l_partial, hq, head_dim, out=
                                      _ptr(l_partial), hq, head_dim, _ptr(out), _ptr(lse),
                                      _stream(stream, dev)), "sa_combine")
     return out, lse
+
+
+def sa_forward_combine(q, k_pages, v_pages, index: Index, selected, cu_seqlens_q_host,
+                       cu_seqlens_q, used_kv_lens, block_tables, hq, head_dim, block_size,
+                       page_size, softmax_scale, causal, split_edges=0, partials=None, out=None,
+                       lse=None, with_lse=True, path=PATH_AUTO, stream=None):
+    """Steps 2 and 3 on a built index (the fused decode kernel where it
+    applies).  Returns (out, lse, (o, m, l))."""
+    _require(q, torch.float32, "q")
+    dev = q.device
+    kvd = _kv_dtype(k_pages)
+    c = index.c
+    hkv = c.hkv
+    cu_h = _host_i64(cu_seqlens_q_host)
+    rows = partial_rows(index, hq) if hkv > 0 and hq % max(hkv, 1) == 0 else 1
+    if partials is None:
+        partials = (torch.empty((rows, head_dim), dtype=torch.float32, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev))
+    if out is None:
+        out = torch.empty((c.tq, hq, head_dim), dtype=torch.float32, device=dev)
+    if lse is None and with_lse:
+        lse = torch.empty((c.tq, hq), dtype=torch.float32, device=dev)
+    page_elems = hkv * page_size * head_dim
+    num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
+    o, m, l = partials
+    _check(_native.load().sa_forward_combine(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(c), _ptr(selected),
+        cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
+        _ptr(block_tables), hq, head_dim, block_size, page_size, softmax_scale,
+        int(bool(causal)), split_edges, _ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path,
+        _stream(stream, dev)), "sa_forward_combine")
+    return out, lse, partials
 
 
 def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens,

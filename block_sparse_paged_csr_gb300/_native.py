@@ -15,11 +15,12 @@ STATUS_NAMES = {
     10: "UNSUPPORTED", 11: "INVALID_ARGUMENT",
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL = 0, 1, 2, 3
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL, PATH_FUSED_DECODE = 0, 1, 2, 3, 4
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",
-           "sa_build_index_no_alloc", "sa_forward", "sa_forward_kernel_name", "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status")
+           "sa_build_index_no_alloc", "sa_forward", "sa_forward_combine", "sa_forward_kernel_name",
+           "sa_attention_kernel_name", "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status")
 
 
 class SaIndex(ctypes.Structure):
@@ -84,8 +85,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_forward.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, i32, i32, i32,
                                i32, i32, f32, i32, p, p, p, st, p]
     lib.sa_forward.restype = st
-    lib.sa_forward_kernel_name.argtypes = [ctypes.POINTER(SaIndex), i32, i32, i32, i32, st, st]
+    lib.sa_forward_combine.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, p, p,
+                                       i32, i32, i32, i32, f32, i32, i32, p, p, p, p, p, st, p]
+    lib.sa_forward_combine.restype = st
+    lib.sa_forward_kernel_name.argtypes = [i64, i32, i32, i32, i32, i32, i32, st, st]
     lib.sa_forward_kernel_name.restype = ctypes.c_char_p
+    lib.sa_attention_kernel_name.argtypes = [i64, i32, p, i64, i32, i32, i32, i32, i32, st, st]
+    lib.sa_attention_kernel_name.restype = ctypes.c_char_p
     lib.sa_combine.argtypes = [ctypes.POINTER(SaIndex), p, p, p, i32, i32, p, p, p]
     lib.sa_combine.restype = st
     lib.sa_attention.argtypes = [p, p, p, i64, st, p, i64, i32, p, p, i32, p, p, i32, i32, i32,

@@ -36,9 +36,9 @@ enum class FwdKernel { kNone, kGeneral, kDecode, kDecodeMma, kTensor };
 // the per-warp decode kernels (warp-level MMA for bf16 K/V, f32 FMA
 // otherwise); problems whose units gather many rows go to the tcgen05
 // kernel; the general f32 kernel takes whatever the others do not support.
-FwdKernel choose_forward(const sa_index* idx, int32_t qhead, int32_t head_dim,
+FwdKernel choose_forward(int64_t tq, int32_t batch, int32_t qhead, int32_t head_dim,
                          int32_t block_size, int32_t page_size, int kv_bf16, sa_path path) {
-  const bool decode_like = idx->tq <= 2 * static_cast<int64_t>(idx->batch);
+  const bool decode_like = tq <= 2 * static_cast<int64_t>(batch);
   const bool tc_ok = sa::forward_tc_supported(head_dim, block_size, page_size, qhead);
   const bool mma_ok =
       sa::forward_dec_mma_supported(head_dim, block_size, page_size, qhead, kv_bf16);
@@ -61,6 +61,32 @@ FwdKernel choose_forward(const sa_index* idx, int32_t qhead, int32_t head_dim,
       return FwdKernel::kGeneral;
     default:
       return FwdKernel::kNone;
+  }
+}
+
+// Whether steps 2 and 3 run as the fused decode kernel: every sequence holds
+// at most one query (then each work unit carries edges of one query only)
+// and the shape is one the kernel supports.
+bool fused_eligible(int64_t tq, int32_t batch, const int64_t* cu_host, int64_t num_pages,
+                    int32_t hq, int32_t hkv, int32_t head_dim, int32_t block_size,
+                    int32_t page_size, int kv_bf16) {
+  if (cu_host == nullptr || batch < 1 || tq < 1 || hkv < 1 || hq % hkv != 0) return false;
+  if (!sa::fused_dec_supported(head_dim, block_size, page_size, hq / hkv, kv_bf16)) return false;
+  if (num_pages < 1 || num_pages > sa::kFusedMaxRows / (static_cast<int64_t>(hkv) * page_size))
+    return false;
+  if (tq * hq * 4 > sa::kFusedMaxRows) return false;
+  for (int32_t b = 0; b < batch; ++b)
+    if (cu_host[b + 1] - cu_host[b] > 1) return false;
+  return true;
+}
+
+const char* forward_kernel_name(FwdKernel k) {
+  switch (k) {
+    case FwdKernel::kDecodeMma: return "forward_dec_mma_kernel";
+    case FwdKernel::kTensor: return "forward_tc_kernel";
+    case FwdKernel::kDecode: return "forward_dec_kernel";
+    case FwdKernel::kGeneral: return "forward_cc_kernel";
+    default: return nullptr;
   }
 }
 
@@ -135,7 +161,8 @@ sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t ba
   out->splits = 4 * n;
   out->totals = 4;
   out->workspace_bytes =
-      sa::workspace_layout(hkv, batch, sa::index_hist_slot_bound(tq, topk), static_cast<int32_t>(msb))
+      sa::workspace_layout(hkv, batch, tq, sa::index_hist_slot_bound(tq, topk),
+                           static_cast<int32_t>(msb))
           .total;
   return SA_OK;
 }
@@ -165,7 +192,7 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   const int64_t chunks_per_head =
       sa::index_chunks_per_head(cu_seqlens_q_host, batch, topk, &multi_slots);
   const sa::WorkspaceLayout lay =
-      sa::workspace_layout(hkv, batch, multi_slots, static_cast<int32_t>(msb));
+      sa::workspace_layout(hkv, batch, tq, multi_slots, static_cast<int32_t>(msb));
   if (idx->workspace_bytes < lay.total) return SA_ERR_INVALID_ARGUMENT;
 
   idx->tq = tq;
@@ -215,11 +242,12 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   if (num_pages < 0) return SA_ERR_SHAPE;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
+  if (path == SA_PATH_FUSED_DECODE) return SA_ERR_UNSUPPORTED;   // writes no partials
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
       path != SA_PATH_TENSOR_CORE)
     return SA_ERR_INVALID_ARGUMENT;
-  const FwdKernel kernel =
-      choose_forward(idx, hq / hkv, head_dim, block_size, page_size, kv_bf16, path);
+  const FwdKernel kernel = choose_forward(idx->tq, idx->batch, hq / hkv, head_dim, block_size,
+                                          page_size, kv_bf16, path);
   if (kernel == FwdKernel::kNone) return SA_ERR_UNSUPPORTED;
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !o_partial || !m_partial ||
       !l_partial)
@@ -272,21 +300,34 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-const char* sa_forward_kernel_name(const sa_index* idx, int32_t hq, int32_t head_dim,
-                                   int32_t block_size, int32_t page_size, sa_dtype kv_dtype,
-                                   sa_path path) {
-  if (idx == nullptr || idx->hkv <= 0 || hq <= 0 || hq % idx->hkv != 0) return nullptr;
+const char* sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_t hkv,
+                                   int32_t head_dim, int32_t block_size, int32_t page_size,
+                                   sa_dtype kv_dtype, sa_path path) {
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return nullptr;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return nullptr;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return nullptr;
-  switch (choose_forward(idx, hq / idx->hkv, head_dim, block_size, page_size,
-                         kv_dtype == SA_DTYPE_BF16 ? 1 : 0, path)) {
-    case FwdKernel::kDecodeMma: return "forward_dec_mma_kernel";
-    case FwdKernel::kTensor: return "forward_tc_kernel";
-    case FwdKernel::kDecode: return "forward_dec_kernel";
-    case FwdKernel::kGeneral: return "forward_cc_kernel";
-    default: return nullptr;
+  return forward_kernel_name(choose_forward(tq, batch, hq / hkv, head_dim, block_size, page_size,
+                                            kv_dtype == SA_DTYPE_BF16 ? 1 : 0, path));
+}
+
+const char* sa_attention_kernel_name(int64_t tq, int32_t batch, const int64_t* cu_seqlens_q_host,
+                                     int64_t num_pages, int32_t hq, int32_t hkv,
+                                     int32_t head_dim, int32_t block_size, int32_t page_size,
+                                     sa_dtype kv_dtype, sa_path path) {
+  if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return nullptr;
+  const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
+  if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
+    if (hkv > 0 && hq > 0 && hq % hkv == 0 && head_dim > 0 && block_size > 0 && page_size > 0 &&
+        block_size % page_size == 0 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK &&
+        cu_seqlens_q_host[batch] == tq &&
+        fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim, block_size,
+                       page_size, kv_bf16))
+      return "fused_dec_kernel";
+    if (path == SA_PATH_FUSED_DECODE) return nullptr;
   }
+  return sa_forward_kernel_name(tq, batch, hq, hkv, head_dim, block_size, page_size, kv_dtype,
+                                path);
 }
 
 sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m_partial,
@@ -315,6 +356,99 @@ sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
+sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_pages,
+                             int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                             const int32_t* selected, const int64_t* cu_seqlens_q_host,
+                             const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                             const int32_t* block_tables, int32_t hq, int32_t head_dim,
+                             int32_t block_size, int32_t page_size, float softmax_scale,
+                             int32_t causal, int32_t split_edges, float* o_partial,
+                             float* m_partial, float* l_partial, float* out, float* lse,
+                             sa_path path, void* stream) {
+  if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  const int32_t hkv = idx->hkv;
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
+  if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
+    return SA_ERR_BLOCK_PAGE;
+  if (idx->block_size != block_size || idx->page_size != page_size) return SA_ERR_SHAPE;
+  if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
+  if (split_edges < 0) return SA_ERR_INVALID_ARGUMENT;
+  const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
+  const int64_t tq = idx->tq;
+  const int32_t batch = idx->batch;
+  bool fused = false;
+  if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
+    if (validate_cu_host(cu_seqlens_q_host, batch) == SA_OK && cu_seqlens_q_host[batch] == tq)
+      fused = fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim,
+                             block_size, page_size, kv_bf16);
+    if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
+  }
+  if (!fused) {
+    const sa_status st = sa_forward(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables,
+                                    cu_seqlens_q, used_kv_lens, hq, hkv, head_dim, block_size,
+                                    page_size, softmax_scale, causal, o_partial, m_partial,
+                                    l_partial, path, stream);
+    if (st != SA_OK) return st;
+    return sa_combine(idx, o_partial, m_partial, l_partial, hq, head_dim, out, lse, stream);
+  }
+  if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !selected || !o_partial ||
+      !m_partial || !l_partial || !out || !idx->inv || !idx->workspace || !idx->totals)
+    return SA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o_partial) ||
+      !aligned16(out))
+    return SA_ERR_INVALID_ARGUMENT;
+  if (idx->msb <= 0) return SA_ERR_SHAPE;   // a built index over these sizes addresses blocks
+  sa::FusedDecArgs a{};
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.num_pages = num_pages;
+  a.kv_bf16 = kv_bf16;
+  a.block_tables = block_tables;
+  a.cu = cu_seqlens_q;
+  a.used = used_kv_lens;
+  a.selected = selected;
+  a.inv = idx->inv;
+  a.tq = tq;
+  a.batch = batch;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.qhead = hq / hkv;
+  a.topk = idx->topk;
+  a.block_size = block_size;
+  a.page_size = page_size;
+  a.pages_per_block = block_size / page_size;
+  a.max_pages = idx->max_pages;
+  a.msb = idx->msb;
+  // Ranks per piece: split_edges when given (at most 32), else enough pieces
+  // for about twelve per SM.
+  int ep = split_edges;
+  if (ep <= 0) {
+    const int64_t items = tq * hkv;
+    const int64_t want = 12 * static_cast<int64_t>(sa::device_sm_count());
+    int64_t p = (want + items - 1) / items;
+    if (p > a.topk) p = a.topk;
+    if (p < 1) p = 1;
+    ep = static_cast<int>((a.topk + p - 1) / p);
+  }
+  if (ep > 32) ep = 32;
+  a.ranks_per_piece = ep;
+  a.pieces = (a.topk + ep - 1) / ep;
+  a.scale = softmax_scale;
+  a.status = idx->totals + 3;
+  a.item_cnt = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(idx->workspace) +
+                                           sa::workspace_layout(hkv, batch, tq, 0, 1).item_cnt);
+  a.part_o = o_partial;
+  a.part_m = m_partial;
+  a.part_l = l_partial;
+  a.out = out;
+  a.lse = lse;
+  (void)causal;   // a no-op for one query per sequence (its position is lk - 1)
+  const cudaError_t err = sa::launch_fused_dec(a, static_cast<cudaStream_t>(stream));
+  if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
 sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
                        int64_t num_pages, sa_dtype kv_dtype, const int32_t* selected, int64_t tq,
                        int32_t topk, const int64_t* cu_seqlens_q_host,
@@ -327,19 +461,28 @@ sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return SA_ERR_BLOCK_PAGE;
-  if (!sa::forward_cc_supported(head_dim, block_size, kv_dtype == SA_DTYPE_BF16) &&
+  if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
+  const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
+  // Shape checks of the forward step, before any device work.
+  bool fused = false;
+  if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
+    if (tq > 0 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK)
+      fused = fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim,
+                             block_size, page_size, kv_bf16);
+    if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
+  }
+  if (!fused && !sa::forward_cc_supported(head_dim, block_size, kv_bf16) &&
       !(path == SA_PATH_TENSOR_CORE &&
         sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv)))
     return SA_ERR_UNSUPPORTED;
-  sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q, batch,
-                                used_kv_lens, max_pages, block_size, page_size, split_edges, idx,
-                                stream);
+  const sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q,
+                                      batch, used_kv_lens, max_pages, block_size, page_size,
+                                      split_edges, idx, stream);
   if (st != SA_OK) return st;
-  st = sa_forward(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables, cu_seqlens_q,
-                  used_kv_lens, hq, hkv, head_dim, block_size, page_size, softmax_scale, causal,
-                  o_partial, m_partial, l_partial, path, stream);
-  if (st != SA_OK) return st;
-  return sa_combine(idx, o_partial, m_partial, l_partial, hq, head_dim, out, lse, stream);
+  return sa_forward_combine(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                            cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                            head_dim, block_size, page_size, softmax_scale, causal, split_edges,
+                            o_partial, m_partial, l_partial, out, lse, path, stream);
 }
 
 sa_status sa_get_status(const sa_index* idx, void* stream) {

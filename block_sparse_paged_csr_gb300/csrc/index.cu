@@ -529,15 +529,16 @@ int64_t index_hist_slot_bound(int64_t tq, int32_t topk) {
   return 2 * (tq * topk) / kChunkEntries + 1;
 }
 
-WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t hist_slots_per_head,
-                                 int32_t msb) {
+WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
+                                 int64_t hist_slots_per_head, int32_t msb) {
   WorkspaceLayout L{};
   const size_t nseg = static_cast<size_t>(hkv) * batch;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   L.barrier = 0;
   L.seg_done = 256;
-  L.seg_tot = up(L.seg_done + 4 * nseg);
-  L.zero_bytes = L.seg_tot;                       // barrier and per-segment counters
+  L.item_cnt = up(L.seg_done + 4 * nseg);
+  L.seg_tot = up(L.item_cnt + 4 * static_cast<size_t>(hkv) * static_cast<size_t>(tq));
+  L.zero_bytes = L.seg_tot;                       // barrier and counters
   L.seg_pre = up(L.seg_tot + 12 * nseg);
   L.hist = up(L.seg_pre + 24 * (nseg + 1));
   L.total = up(L.hist + 4 * static_cast<size_t>(hkv) * static_cast<size_t>(hist_slots_per_head) *
@@ -547,7 +548,8 @@ WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t hist_slots_
 
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
                                int64_t hist_slots_per_head, cudaStream_t stream) {
-  const WorkspaceLayout lay = workspace_layout(a.hkv, a.batch, hist_slots_per_head, a.msb);
+  const WorkspaceLayout lay =
+      workspace_layout(a.hkv, a.batch, a.tq, hist_slots_per_head, a.msb);
   cudaError_t err = cudaMemsetAsync(a.idx.workspace, 0, lay.zero_bytes, stream);
   if (err != cudaSuccess) return err;
   const size_t smem = index_smem_bytes(a.msb, a.batch, a.hkv);

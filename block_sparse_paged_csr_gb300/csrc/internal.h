@@ -17,6 +17,7 @@ constexpr int kChunkEntries = 4096;
 struct WorkspaceLayout {
   size_t barrier;       // uint32[2]: grid barrier counter and generation
   size_t seg_done;      // uint32[hkv*batch]: chunks of the segment that finished phase 1
+  size_t item_cnt;      // uint32[tq*hkv]: finished pieces per (query, kv head), fused decode
   size_t seg_tot;       // int32[hkv*batch][3]: edges, non-empty bins, work splits
   size_t seg_pre;       // int64[hkv*batch+1][3]: exclusive prefixes of seg_tot
   size_t hist;          // int32[hkv][slots][msb]: histograms of multi-chunk segments
@@ -24,8 +25,8 @@ struct WorkspaceLayout {
   size_t total;
 };
 
-WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t hist_slots_per_head,
-                                 int32_t msb);
+WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
+                                 int64_t hist_slots_per_head, int32_t msb);
 // Chunks of one head (and, in *multi_slots, chunks of its multi-chunk segments).
 int64_t index_chunks_per_head(const int64_t* cu_host, int32_t batch, int32_t topk,
                               int64_t* multi_slots);
@@ -89,6 +90,40 @@ bool forward_dec_mma_supported(int head_dim, int block_size, int page_size, int 
 // Pipelined decode-shaped forward (head_dim 128, few rows per split).
 cudaError_t launch_forward_dec(const ForwardArgs& a, cudaStream_t stream);
 bool forward_dec_supported(int head_dim, int block_size, int page_size, int qhead, int kv_bf16);
+
+// Fused decode attention (forward and combine in one kernel) for batches in
+// which every sequence holds at most one query.
+struct FusedDecArgs {
+  const float* q;
+  const void* k_pages;
+  const void* v_pages;
+  int64_t num_pages;
+  int kv_bf16;
+  const int32_t* block_tables;
+  const int64_t* cu;
+  const int32_t* used;      // nullable
+  const int32_t* selected;  // [tq, hkv, topk]
+  const int32_t* inv;       // [hkv, tq, topk] of the built index
+  int64_t tq;
+  int32_t batch, hq, hkv, qhead, topk, block_size, page_size, pages_per_block, max_pages, msb;
+  int32_t pieces;           // pieces per (query, kv head)
+  int32_t ranks_per_piece;  // at most 32
+  float scale;
+  int64_t* status;          // device status word
+  uint32_t* item_cnt;       // [tq * hkv], zero on entry, left zero
+  float* part_o;            // per-piece scratch rows (the partial buffers)
+  float* part_m;
+  float* part_l;
+  float* out;
+  float* lse;               // nullable
+};
+
+// Whether the fused decode kernel supports this shape (the caller also checks
+// that every sequence holds at most one query and the pool size limits).
+bool fused_dec_supported(int head_dim, int block_size, int page_size, int qhead, int kv_bf16);
+// Largest pool (num_pages * hkv * page_size key rows) the kernel addresses.
+constexpr int64_t kFusedMaxRows = (int64_t{1} << 31) - 1;
+cudaError_t launch_fused_dec(const FusedDecArgs& a, cudaStream_t stream);
 
 struct CombineArgs {
   const int32_t* inv;

@@ -62,7 +62,7 @@ extern "C" sa_status sa_build_index_no_alloc(const int32_t* selected, int64_t tq
     int64_t multi_slots = 0;
     sa::index_chunks_per_head(cu_seqlens_q_host, batch, topk, &multi_slots);
     const int64_t msb = max_pages / (block_size / page_size);
-    if (sa::workspace_layout(hkv, batch, multi_slots, static_cast<int32_t>(msb)).total >
+    if (sa::workspace_layout(hkv, batch, tq, multi_slots, static_cast<int32_t>(msb)).total >
         kStaticScratchBytes)
       return SA_ERR_UNSUPPORTED;  // the problem needs more scratch than the array holds
   }

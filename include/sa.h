@@ -10,7 +10,8 @@
  *      kvouter_forward / process_work_unit
  *   3. sa_combine:     merge each (query, q-head)'s partials with the
  *      log-sum-exp rule                              - forward.rs, module doc
- * sa_attention runs the three in sequence on one stream with no host sync.
+ * sa_attention runs the three in sequence on one stream with no host sync;
+ * sa_forward_combine runs steps 2 and 3 on a built index.
  *
  * Conventions for every entry point:
  *   - Array arguments are DEVICE pointers unless the name ends in _host.  The
@@ -72,7 +73,12 @@ typedef enum sa_path {
                                     tcgen05 kernel (block 64 or 128, qhead dividing
                                     128, bf16 operands); f32 accumulation;
                                     SA_ERR_UNSUPPORTED elsewhere                   */
-  SA_PATH_CUDA_CORE_GENERAL = 3  /* the general f32 FMA kernel only                 */
+  SA_PATH_CUDA_CORE_GENERAL = 3, /* the general f32 FMA kernel only                 */
+  SA_PATH_FUSED_DECODE = 4       /* sa_attention / sa_forward_combine only: forward
+                                    and combine as one kernel when every sequence
+                                    holds at most one query (see sa_attention);
+                                    SA_ERR_UNSUPPORTED elsewhere and from
+                                    sa_forward                                   */
 } sa_path;
 
 /*
@@ -247,17 +253,48 @@ sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
                      void *stream);
 
 /*
- * Name of the kernel sa_forward would launch for these arguments and `path`
+ * Name of the kernel sa_forward launches for a problem of tq queries in
+ * `batch` sequences with these head counts, sizes, K/V type and `path`
  * ("forward_dec_mma_kernel", "forward_tc_kernel", "forward_dec_kernel" or
- * "forward_cc_kernel"), or NULL where sa_forward would refuse them (bad head
- * counts or block/page sizes, or SA_ERR_UNSUPPORTED).  Host only: reads the
- * geometry fields of idx (hkv, tq, batch), touches no device memory.  The
- * pages have no counterpart; it lets a caller (or a profiler script) know which
- * kernel serves a problem shape.  The returned string is static.
+ * "forward_cc_kernel"), or NULL where sa_forward would refuse it (bad head
+ * counts or block/page sizes, or SA_ERR_UNSUPPORTED).  Host only; the returned
+ * string is static.  The pages have no counterpart: it tells a caller (or a
+ * profiling script) which kernel serves a shape.
  */
-const char *sa_forward_kernel_name(const sa_index *idx, int32_t hq, int32_t head_dim,
-                                   int32_t block_size, int32_t page_size, sa_dtype kv_dtype,
-                                   sa_path path);
+const char *sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_t hkv,
+                                   int32_t head_dim, int32_t block_size, int32_t page_size,
+                                   sa_dtype kv_dtype, sa_path path);
+
+/*
+ * The kernel that sa_attention / sa_forward_combine run for steps 2 and 3:
+ * "fused_dec_kernel" on the fused decode path (see sa_attention), else the
+ * name sa_forward_kernel_name gives; NULL where the shape would be refused.
+ * Host only (reads cu_seqlens_q_host[0..batch]).
+ */
+const char *sa_attention_kernel_name(int64_t tq, int32_t batch, const int64_t *cu_seqlens_q_host,
+                                     int64_t num_pages, int32_t hq, int32_t hkv,
+                                     int32_t head_dim, int32_t block_size, int32_t page_size,
+                                     sa_dtype kv_dtype, sa_path path);
+
+/*
+ * Steps 2 and 3 on an index built by sa_build_index (same stream), with no
+ * host synchronisation: the forward and the combine, or, on the fused decode
+ * path described at sa_attention, the one kernel that does both.  Arguments
+ * as for sa_forward and sa_combine, plus `selected` and cu_seqlens_q_host
+ * (those given to sa_build_index) and split_edges (used by the fused path
+ * only: ranks per piece).  The partial buffers are scratch on the fused path.
+ * Errors as for sa_forward and sa_combine; SA_ERR_SHAPE when the index's
+ * block or page size differ from the arguments.
+ */
+sa_status sa_forward_combine(const float *q, const void *k_pages, const void *v_pages,
+                             int64_t num_pages, sa_dtype kv_dtype, const sa_index *idx,
+                             const int32_t *selected, const int64_t *cu_seqlens_q_host,
+                             const int64_t *cu_seqlens_q, const int32_t *used_kv_lens,
+                             const int32_t *block_tables, int32_t hq, int32_t head_dim,
+                             int32_t block_size, int32_t page_size, float softmax_scale,
+                             int32_t causal, int32_t split_edges, float *o_partial,
+                             float *m_partial, float *l_partial, float *out, float *lse,
+                             sa_path path, void *stream);
 
 /*
  * Step 3: log-sum-exp combine (forward.rs module doc: "standard FlashAttention
@@ -278,6 +315,19 @@ sa_status sa_combine(const sa_index *idx, const float *o_partial, const float *m
  * fused public entry of the module).  Arguments as above; `idx` carries the
  * caller's index arrays and workspace and is filled in as by sa_build_index.
  * The partial buffers are scratch of the sizes sa_forward documents.
+ *
+ * Fused decode path (SA_PATH_AUTO or SA_PATH_FUSED_DECODE): when every
+ * sequence holds at most one query (cu_seqlens_q_host), head_dim is 128,
+ * page_size is a power of two of at least 8, block_size / page_size <= 8,
+ * block_size <= 64 or a multiple of 64, qhead <= 4 (f32 K/V) or <= 16 (bf16),
+ * num_pages * hkv * page_size < 2^31 and tq * hq * 4 < 2^31, steps 2 and 3
+ * run as one kernel that keeps each query's partials on chip: every work
+ * unit of such a batch carries edges of a single query, so the combine only
+ * ever merges a (query, kv head)'s own units.  The index is still built in
+ * full.  The kernel splits each (query, kv head)'s ranks into pieces of
+ * split_edges ranks (at most 32; 0 = chosen from the SM count) and merges the
+ * pieces through rows of the partial buffers, whose content afterwards is
+ * unspecified.  out and lse equal those of the unfused path up to rounding.
  */
 sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,
                        int64_t num_pages, sa_dtype kv_dtype, const int32_t *selected,

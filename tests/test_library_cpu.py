@@ -156,3 +156,36 @@ def test_forward_kernel_choice(lib):
     assert name(4, 1, 3, 4, 32, 32, 16) is None
     assert name(4, 1, 2, 4, 32, 32, 24) is None
     assert name(4, 1, 2, 4, 512, 32, 16) is None
+
+
+def test_attention_kernel_choice(lib):
+    """sa_attention's steps 2-3: the fused decode kernel exactly when every
+    sequence holds at most one query and the shape is supported."""
+    import block_sparse_paged_csr_gb300 as sa
+    import inputs
+
+    name = sa.sa_attention_kernel_name
+    for wname, fused in (("gqa_decode", True), ("long_decode", True), ("chunked_prefill", False),
+                         ("skewed", False), ("tiny", False)):
+        w = inputs.FULL[wname]()
+        got = name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq, w.head_dim, w.block_size,
+                   w.page_size, w.kv_dtype)
+        want = "fused_dec_kernel" if fused else sa.sa_forward_kernel_name(
+            w.tq, w.batch, w.hkv, w.hq, w.head_dim, w.block_size, w.page_size, w.kv_dtype)
+        assert got == want, (wname, got)
+    one = np.array([0, 1, 1, 2, 3], np.int64)          # an empty sequence is allowed
+    two = np.array([0, 1, 3, 4], np.int64)             # a sequence with two queries is not
+    geo = (1000, 8, 32, 128, 64, 16)
+    assert name(one, *geo, "f32") == "fused_dec_kernel"
+    assert name(one, *geo, "bf16", sa.PATH_FUSED_DECODE) == "fused_dec_kernel"
+    assert name(two, *geo, "f32") == "forward_dec_kernel"
+    assert name(two, *geo, "f32", sa.PATH_FUSED_DECODE) is None
+    assert name(one, *geo, "f32", sa.PATH_CUDA_CORE) == "forward_dec_kernel"
+    # f32 up to 4 q-heads per kv head, bf16 up to 16
+    assert name(one, 1000, 8, 64, 128, 64, 16, "f32") == "forward_dec_kernel"
+    assert name(one, 1000, 8, 64, 128, 64, 16, "bf16") == "fused_dec_kernel"
+    # pages of fewer than 8 keys, or not a power of two, are not fused
+    assert name(one, 1000, 8, 32, 128, 64, 4, "f32") != "fused_dec_kernel"
+    assert name(one, 1000, 8, 32, 128, 48, 24, "f32") != "fused_dec_kernel"
+    # head_dim 128 only
+    assert name(one, 1000, 8, 32, 64, 64, 16, "f32") == "forward_cc_kernel"

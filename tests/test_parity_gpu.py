@@ -39,8 +39,9 @@ def test_small_workload_parity(name, split):
     _gpu.compare_index(idx.to_host(), ref_idx)
     rows = ref_idx["edges"].shape[0] * w.qhead
     tol = _gpu.auto_tol(w)
-    _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(), l[:rows].cpu().numpy(),
-                          ro, rm, rl, tol)
+    if not _gpu.uses_fused(w):      # the fused decode path keeps its partials on chip
+        _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(),
+                              l[:rows].cpu().numpy(), ro, rm, rl, tol)
     assert _gpu.row_error(out.cpu().numpy(), ref_out) <= tol
     _gpu.compare_lse(lse.cpu().numpy(), ref_lse, tol)
 
@@ -83,8 +84,13 @@ def test_random_edge_cases(seed):
             c["bs"], c["ps"], c["scale"], causal, split_edges=split)
         _gpu.compare_index(idx.to_host(), ref_idx)
         rows = ref_idx["edges"].shape[0] * (c["hq"] // c["hkv"])
-        _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(),
-                              l[:rows].cpu().numpy(), ro, rm, rl, _gpu.TOL_F32)
+        num_pages = t["k"].numel() // (c["hkv"] * c["ps"] * c["d"])
+        fused = sa.sa_attention_kernel_name(
+            c["cu"], num_pages, c["hkv"], c["hq"], c["d"], c["bs"], c["ps"],
+            "bf16" if bf16 else "f32") == "fused_dec_kernel"
+        if not fused:
+            _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(),
+                                  l[:rows].cpu().numpy(), ro, rm, rl, _gpu.TOL_F32)
         assert _gpu.row_error(out.cpu().numpy(), ref_out) <= _gpu.TOL_F32
         _gpu.compare_lse(lse.cpu().numpy(), ref_lse, _gpu.TOL_F32)
 
