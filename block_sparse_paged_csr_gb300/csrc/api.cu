@@ -420,18 +420,27 @@ sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_
   a.pages_per_block = block_size / page_size;
   a.max_pages = idx->max_pages;
   a.msb = idx->msb;
-  // Ranks per piece: split_edges when given (at most 32), else enough pieces
-  // for about twelve per SM.
+  // Pieces.  split_edges > 0: every pair in pieces of split_edges ranks (at
+  // most 64).  Otherwise whole pairs (all ranks, when topk <= 64) round-robin
+  // over the SMs, and only the pairs of the last, partial round are cut, into
+  // as many pieces as keep the otherwise idle SMs busy.
+  const int64_t items = tq * hkv;
   int ep = split_edges;
+  a.whole_items = 0;
   if (ep <= 0) {
-    const int64_t items = tq * hkv;
-    const int64_t want = 12 * static_cast<int64_t>(sa::device_sm_count());
-    int64_t p = (want + items - 1) / items;
-    if (p > a.topk) p = a.topk;
-    if (p < 1) p = 1;
-    ep = static_cast<int>((a.topk + p - 1) / p);
+    if (a.topk <= 64) {
+      const int64_t sms = sa::device_sm_count();
+      const int64_t tail = items % sms;
+      int64_t pt = tail > 0 ? sms / tail : 1;
+      if (pt > a.topk) pt = a.topk;
+      if (pt < 1) pt = 1;
+      a.whole_items = pt == 1 ? items : items - tail;
+      ep = static_cast<int>((a.topk + pt - 1) / pt);
+    } else {
+      ep = 64;
+    }
   }
-  if (ep > 32) ep = 32;
+  if (ep > 64) ep = 64;
   a.ranks_per_piece = ep;
   a.pieces = (a.topk + ep - 1) / ep;
   a.scale = softmax_scale;

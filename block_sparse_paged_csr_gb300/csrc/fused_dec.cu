@@ -7,10 +7,12 @@
 // of that query only, so all partials the combine merges for a (query, kv
 // head) pair come from the pair's own kept ranks.  The kernel therefore walks
 // the kept ranks of each pair and keeps the merge on chip: a "piece" is a
-// range of ranks of one pair; its blocks stream through shared memory and one
-// online softmax runs across them.  Pieces of one pair meet in a small global
-// scratch (one (o, m, l) row per piece and GQA lane, normally still in L2);
-// the last piece of the pair to finish merges them and writes out and lse.
+// range of ranks of one pair (normally all of them); its blocks stream through
+// shared memory and one online softmax runs across them.  Where a pair is cut
+// into several pieces (to fill the SMs in the last round of pairs, or when
+// asked), they meet in a small global scratch (one (o, m, l) row per piece and
+// GQA lane, normally still in L2); the last piece of the pair to finish
+// merges them and writes out and lse.
 // The causal mask is a no-op here: a sequence's only query sits at position
 // lk - 1 and sees every key below lk.
 //
@@ -18,18 +20,26 @@
 //   warp 0    metadata: for each piece the query's sequence and KV length,
 //             the kept ranks (inv >= 0) with their blocks and page ids, into
 //             a ring of piece descriptors in shared memory;
-//   warp 1    loads: for each 64-key chunk of a kept block, tensor-map copies
+//   warps 1-2 loads: for each 64-key chunk of a kept block, tensor-map copies
 //             of its K and V pages with the 128-byte swizzle, plus the piece's
-//             Q rows, into a ring of stages;
-//   warps 2.. consumers: each owns a slice of every chunk's keys and keeps its
+//             Q rows, into a ring of stages (the two warps take alternate
+//             stages: the copies one warp issues alone fall well short of HBM
+//             bandwidth);
+//   warp 3    merge: merges the consumers' states of a finished piece and
+//             writes the output (or the piece's scratch rows, the pair's
+//             counter and, for the pair's last piece, the merge of its
+//             scratch rows), beside the consumers;
+//   warps 4.. consumers: each owns a slice of every chunk's keys and keeps its
 //             own online-softmax state over the piece; at the end of a piece
-//             the states are merged through shared memory.
+//             they hand the states to the merge warp through shared memory
+//             and go on (they wait for it only at their next piece's end).
 // f32 K/V: 8 consumer warps x 8 keys on CUDA-core FMA; the piece's Q rows
 // come with every stage (a 2 KB copy, from L2 after the first) in the same
 // swizzled layout, so the scores read Q from shared memory without bank
 // conflicts and hold no Q in registers.  bf16 K/V: 4 consumer warps x 16 keys
 // on warp-level MMA (m16n8k16), Q and P split into bf16 high parts and
-// remainders, Q fragments in registers from the piece's first stage.
+// remainders; with at most 8 q-heads per kv head the remainders ride in the
+// tile's otherwise empty rows 8-15, so the split costs no extra MMA.
 //
 // Shared-memory layout of a stage (a 1024-byte aligned region per tensor):
 //   f32:  [key][quarter of head_dim][32 floats], one 128-byte row per
@@ -49,7 +59,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kCK = 64;              // keys per stage
-constexpr int kMaxEP = 32;           // ranks per piece
+constexpr int kMaxEP = 64;           // ranks per piece
 constexpr int kMaxPPB = 8;           // pages per block
 constexpr int kDescs = 4;            // piece descriptors in flight
 constexpr uint32_t kFirst = 1u, kLast = 2u, kDone = 4u;
@@ -74,8 +84,10 @@ struct StageHdr {
 };
 
 template <bool kBf16> struct Cfg;
-template <> struct Cfg<false> { static constexpr int NC = 8; };   // 8 keys per consumer warp
-template <> struct Cfg<true> { static constexpr int NC = 4; };    // 16 keys per consumer warp
+// NC consumer warps (keys of a stage split between them), NL load warps
+// (stages round-robin: one warp's copy issue alone does not keep HBM busy).
+template <> struct Cfg<false> { static constexpr int NC = 8, NL = 2; };   // 8 keys per consumer
+template <> struct Cfg<true> { static constexpr int NC = 4, NL = 2; };    // 16 keys per consumer
 
 struct Layout {
   uint32_t tensor;     // bytes of K (or V) of one stage
@@ -97,7 +109,7 @@ __host__ __device__ constexpr Layout fused_layout() {
   L.ml = L.mm + Cfg<kBf16>::NC * R * 4;
   L.desc = up_to(L.ml + Cfg<kBf16>::NC * R * 4, 16);
   L.bars = up_to(L.desc + kDescs * static_cast<uint32_t>(sizeof(PieceDesc)), 8);
-  L.flag = L.bars + (2 * S + 2 * kDescs + 1) * 8;
+  L.flag = L.bars + (2 * S + 2 * kDescs + 2) * 8;           // merge info: item, k
   L.total = L.flag + 16;
   return L;
 }
@@ -114,8 +126,9 @@ struct Smem {
   uint64_t* empty;
   uint64_t* dfull;
   uint64_t* dempty;
-  uint64_t* merge;
-  volatile int* flag;
+  uint64_t* mready;     // consumers -> merge warp: the piece's states are in mo/mm/ml
+  uint64_t* mfree;      // merge warp -> consumers: the states have been read
+  volatile int* minfo;  // item, k of the piece being merged (-1: no more pieces)
 };
 
 // ------------------------------------------------------------------ metadata
@@ -153,47 +166,64 @@ __device__ void meta_warp(const FusedDecArgs& a, const Smem& sm, int64_t n_piece
       mbar_arrive(sm.dfull + slot);
       return;
     }
-    const int64_t item = g / a.pieces;
-    const int k = static_cast<int>(g - item * a.pieces);
+    int64_t item;
+    int k, r0, nrange;
+    if (g < a.whole_items) {            // a whole pair: all its ranks
+      item = g;
+      k = 0;
+      r0 = 0;
+      nrange = a.topk;
+    } else {
+      const int64_t t = g - a.whole_items;
+      item = a.whole_items + t / a.pieces;
+      k = static_cast<int>(t - (item - a.whole_items) * a.pieces);
+      r0 = k * a.ranks_per_piece;
+      nrange = min(a.ranks_per_piece, a.topk - r0);
+    }
     const int64_t i = item / a.hkv;
     const int h = static_cast<int>(item - i * a.hkv);
     const int b = warp_batch_of(a.cu, a.batch, i, lane);
     const int lk = a.used ? max(a.used[b], 0) : a.msb * a.block_size;
-    const int r0 = k * a.ranks_per_piece;
-    const int nrange = min(a.ranks_per_piece, a.topk - r0);
-    bool kept = false;
-    int blk = 0;
-    if (lane < nrange) {
-      const int r = r0 + lane;
-      kept = a.inv[(static_cast<int64_t>(h) * a.tq + i) * a.topk + r] >= 0;
-      if (kept) {
-        blk = a.selected[(i * a.hkv + h) * a.topk + r];
-        if (blk < 0 || blk >= a.msb) {      // only after an index that reported an error
-          report(a.status, SA_ERR_SELECTED_RANGE);
-          kept = false;
-        }
-      }
-    }
-    const unsigned km = __ballot_sync(0xffffffffu, kept);
-    if (kept) {
-      const int pos = __popc(km & ((1u << lane) - 1u));
-      d.blk[pos] = blk;
-      const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
-                          static_cast<int64_t>(blk) * a.pages_per_block;
-      const int64_t key0 = static_cast<int64_t>(blk) * a.block_size;
+    // Ranks r0 + lane and r0 + 32 + lane; kept ones compacted in rank order.
+    int nkept = 0;
 #pragma unroll
-      for (int p = 0; p < kMaxPPB; ++p) {
-        int id = -1;
-        if (p < a.pages_per_block && key0 + static_cast<int64_t>(p) * a.page_size < lk) {
-          id = bt[p];
-          if (id >= a.num_pages) {
-            report(a.status, SA_ERR_SHAPE);
-            id = -1;
+    for (int half = 0; half < kMaxEP / 32; ++half) {
+      const int jr = 32 * half + lane;
+      bool kept = false;
+      int blk = 0;
+      if (jr < nrange) {
+        const int r = r0 + jr;
+        kept = a.inv[(static_cast<int64_t>(h) * a.tq + i) * a.topk + r] >= 0;
+        if (kept) {
+          blk = a.selected[(i * a.hkv + h) * a.topk + r];
+          if (blk < 0 || blk >= a.msb) {    // only after an index that reported an error
+            report(a.status, SA_ERR_SELECTED_RANGE);
+            kept = false;
           }
-          if (id < 0) id = -1;
         }
-        d.pid[pos][p] = id;
       }
+      const unsigned km = __ballot_sync(0xffffffffu, kept);
+      if (kept) {
+        const int pos = nkept + __popc(km & ((1u << lane) - 1u));
+        d.blk[pos] = blk;
+        const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
+                            static_cast<int64_t>(blk) * a.pages_per_block;
+        const int64_t key0 = static_cast<int64_t>(blk) * a.block_size;
+#pragma unroll
+        for (int p = 0; p < kMaxPPB; ++p) {
+          int id = -1;
+          if (p < a.pages_per_block && key0 + static_cast<int64_t>(p) * a.page_size < lk) {
+            id = bt[p];
+            if (id >= a.num_pages) {
+              report(a.status, SA_ERR_SHAPE);
+              id = -1;
+            }
+            if (id < 0) id = -1;
+          }
+          d.pid[pos][p] = id;
+        }
+      }
+      nkept += __popc(km);
     }
     if (lane == 0) {
       d.item = static_cast<int>(item);
@@ -201,7 +231,7 @@ __device__ void meta_warp(const FusedDecArgs& a, const Smem& sm, int64_t n_piece
       d.i = static_cast<int>(i);
       d.h = h;
       d.lk = lk;
-      d.nr = __popc(km);
+      d.nr = nkept;
     }
     __syncwarp();
     mbar_arrive(sm.dfull + slot);
@@ -210,9 +240,12 @@ __device__ void meta_warp(const FusedDecArgs& a, const Smem& sm, int64_t n_piece
 
 // ------------------------------------------------------------------ loads
 
+// Load warp lw of NL: fills the stages whose running index is lw modulo NL.
 template <bool kBf16, int R, int S>
-__device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem& sm, int lane) {
+__device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem& sm, int lw,
+                          int lane) {
   constexpr Layout L = fused_layout<kBf16, R, S>();
+  constexpr uint32_t NL = Cfg<kBf16>::NL;
   const int ck = a.block_size < kCK ? a.block_size : kCK;           // keys per chunk
   const int cpb = a.block_size / ck;                                // chunks per block
   const int kb = a.page_size < ck ? a.page_size : ck;               // keys per page box
@@ -230,6 +263,7 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
     const PieceDesc& d = sm.desc[slot];
     const int item = d.item;
     if (item < 0) {
+      if (xs % NL != static_cast<uint32_t>(lw)) break;   // another load warp ends the ring
       const int s = static_cast<int>(xs % S);
       if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u)) {
         ok = false;
@@ -245,6 +279,10 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
     const int nr = d.nr, lk = d.lk, h = d.h;
     const int nst = nr == 0 ? 1 : nr * cpb;
     for (int u = 0; u < nst; ++u) {
+      if (xs % NL != static_cast<uint32_t>(lw)) {    // another load warp's stage
+        ++xs;
+        continue;
+      }
       const int j = u / cpb, c = u - j * cpb;
       const int s = static_cast<int>(xs % S);
       if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u)) {
@@ -319,21 +357,13 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
   }
   if (!ok) {
     if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
-    // Let the copies still in flight land before the CTA can exit.
+    // Let this warp's copies still in flight land before the CTA can exit.
     for (uint32_t x = xs > static_cast<uint32_t>(S) ? xs - S : 0u; x < xs; ++x)
-      mbar_wait_bounded(sm.full + x % S, (x / S) & 1u);
+      if (x % NL == static_cast<uint32_t>(lw)) mbar_wait_bounded(sm.full + x % S, (x / S) & 1u);
   }
 }
 
 // ------------------------------------------------------------------ piece end
-
-// Barrier of all consumer threads (bounded).
-__device__ __forceinline__ bool consumers_sync(const Smem& sm, uint32_t& phase) {
-  mbar_arrive(sm.merge);
-  const bool ok = mbar_wait_bounded(sm.merge, phase & 1u);
-  ++phase;
-  return ok;
-}
 
 __device__ __forceinline__ void write_row(const FusedDecArgs& a, int64_t row, int d4, float m2,
                                           float l, float4 o) {
@@ -343,81 +373,145 @@ __device__ __forceinline__ void write_row(const FusedDecArgs& a, int64_t row, in
   if (a.lse && d4 == 0) a.lse[row] = l > 0.f ? (m2 + log2f(l)) * kLn2 : -INFINITY;
 }
 
-// The warps' states are in sm.mo/mm/ml ([NC][R] rows, m in the log2 domain).
-// Merge them; then either write the output rows (one piece per pair) or the
-// piece's scratch rows, and let the pair's last piece merge the scratch.
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// The merge warp.  Per piece: merge the NC consumer warps' states (m in the
+// log2 domain) row by row, lane = 4 dims; release the state buffer; then
+// either write the output rows (one piece per pair) or the piece's scratch
+// rows, and if this piece is the pair's last to finish (a counter per pair),
+// merge the pair's scratch rows into the output.  It runs beside the
+// consumers, which only wait for it when they hand over their next piece.
 template <int NC, int R>
-__device__ bool finish_piece(const FusedDecArgs& a, const Smem& sm, uint32_t& phase, int item,
-                             int k, int ct) {
-  if (!consumers_sync(sm, phase)) return false;
-  const int64_t i = item / a.hkv;
-  const int h = item - static_cast<int>(i) * a.hkv;
-  const int P = a.pieces;
-  for (int idx = ct; idx < a.qhead * 32; idx += NC * 32) {
-    const int r = idx >> 5, d4 = idx & 31;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NC; ++w) M = fmaxf(M, sm.mm[w * R + r]);
-    float l = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NC; ++w) {
-        const float e = exp2f(sm.mm[w * R + r] - M);
-        l = fmaf(e, sm.ml[w * R + r], l);
-        const float4 v = reinterpret_cast<const float4*>(sm.mo + (w * R + r) * kD)[d4];
-        o.x = fmaf(e, v.x, o.x);
-        o.y = fmaf(e, v.y, o.y);
-        o.z = fmaf(e, v.z, o.z);
-        o.w = fmaf(e, v.w, o.w);
-      }
+__device__ void merge_warp(const FusedDecArgs& a, const Smem& sm, int lane) {
+  const int qhead = a.qhead;
+  for (uint32_t np = 0;; ++np) {
+    if (!mbar_wait_bounded(sm.mready, np & 1u)) {
+      if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
+      return;
     }
-    if (P == 1) {
-      write_row(a, i * a.hq + static_cast<int64_t>(h) * a.qhead + r, d4, M, l, o);
-    } else {
-      const int64_t pr = (static_cast<int64_t>(item) * P + k) * a.qhead + r;
-      reinterpret_cast<float4*>(a.part_o + pr * kD)[d4] = o;
-      if (d4 == 0) {
-        a.part_m[pr] = M;
-        a.part_l[pr] = l;
-      }
-    }
-  }
-  if (P > 1) __threadfence();
-  if (!consumers_sync(sm, phase)) return false;   // also frees sm.mo for the next piece
-  if (P == 1) return true;
-  if (ct == 0) {
-    const unsigned old = atomicAdd(a.item_cnt + item, 1u);
-    const int last = old == static_cast<unsigned>(P - 1);
-    if (last) atomicExch(a.item_cnt + item, 0u);
-    *sm.flag = last;
-  }
-  if (!consumers_sync(sm, phase)) return false;
-  if (*sm.flag) {
-    __threadfence();
-    for (int idx = ct; idx < a.qhead * 32; idx += NC * 32) {
-      const int r = idx >> 5, d4 = idx & 31;
-      const int64_t pr0 = static_cast<int64_t>(item) * P * a.qhead + r;
+    const int item = sm.minfo[0];
+    const int k = sm.minfo[1];
+    if (item < 0) return;
+    const int P = item < a.whole_items ? 1 : a.pieces;
+    const int64_t i = item / a.hkv;
+    const int h = item - static_cast<int>(i) * a.hkv;
+    const int64_t row0 = i * a.hq + static_cast<int64_t>(h) * qhead;
+    // scratch row of (pair, piece kk, lane r): (item * topk + kk) * qhead + r
+    const int64_t prow = static_cast<int64_t>(item) * a.topk * qhead;
+    for (int r = 0; r < qhead; ++r) {
       float M = -INFINITY;
-      for (int kk = 0; kk < P; ++kk) M = fmaxf(M, __ldcg(a.part_m + pr0 + kk * a.qhead));
+#pragma unroll
+      for (int w = 0; w < NC; ++w) M = fmaxf(M, sm.mm[w * R + r]);
       float l = 0.f;
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
       if (M != -INFINITY) {
-        for (int kk = 0; kk < P; ++kk) {
-          const int64_t pr = pr0 + static_cast<int64_t>(kk) * a.qhead;
-          const float e = exp2f(__ldcg(a.part_m + pr) - M);
-          l = fmaf(e, __ldcg(a.part_l + pr), l);
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + pr * kD) + d4);
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+          const float e = exp2f(sm.mm[w * R + r] - M);
+          l = fmaf(e, sm.ml[w * R + r], l);
+          const float4 v = reinterpret_cast<const float4*>(sm.mo + (w * R + r) * kD)[lane];
           o.x = fmaf(e, v.x, o.x);
           o.y = fmaf(e, v.y, o.y);
           o.z = fmaf(e, v.z, o.z);
           o.w = fmaf(e, v.w, o.w);
         }
       }
-      write_row(a, i * a.hq + static_cast<int64_t>(h) * a.qhead + r, d4, M, l, o);
+      if (P == 1) {
+        write_row(a, row0 + r, lane, M, l, o);
+      } else {
+        const int64_t pr = prow + static_cast<int64_t>(k) * qhead + r;
+        reinterpret_cast<float4*>(a.part_o + pr * kD)[lane] = o;
+        if (lane == 0) {
+          a.part_m[pr] = M;
+          a.part_l[pr] = l;
+        }
+      }
+    }
+    __syncwarp();
+    mbar_arrive(sm.mfree);
+    if (P == 1) continue;
+    __threadfence();
+    unsigned last = 0;
+    if (lane == 0) {
+      const unsigned old = atomicAdd(a.item_cnt + item, 1u);
+      last = old == static_cast<unsigned>(P - 1);
+      if (last) atomicExch(a.item_cnt + item, 0u);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    // The pair's P scratch rows per GQA lane: statistics one piece per lane,
+    // then the o rows, eight loads in flight.
+    for (int r = 0; r < qhead; ++r) {
+      const int64_t pr0 = prow + r;
+      float M = -INFINITY;
+      for (int b = 0; b < P; b += 32)
+        if (b + lane < P) M = fmaxf(M, __ldcg(a.part_m + pr0 + static_cast<int64_t>(b + lane) * qhead));
+      M = warp_max(M);
+      float l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        for (int b = 0; b < P; b += 32) {
+          float e = 0.f;
+          if (b + lane < P) {
+            const int64_t pr = pr0 + static_cast<int64_t>(b + lane) * qhead;
+            e = exp2f(__ldcg(a.part_m + pr) - M);
+            l = fmaf(e, __ldcg(a.part_l + pr), l);
+          }
+          const int n = min(32, P - b);
+          for (int t0 = 0; t0 < n; t0 += 8) {
+            float wt[8];
+            float4 v[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              wt[t] = __shfl_sync(0xffffffffu, e, (t0 + t) & 31);
+              v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (t0 + t < n && wt[t] > 0.f)
+                v[t] = __ldcg(reinterpret_cast<const float4*>(
+                                  a.part_o + (pr0 + static_cast<int64_t>(b + t0 + t) * qhead) * kD) +
+                              lane);
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float ww = t0 + t < n ? wt[t] : 0.f;
+              o.x = fmaf(ww, v[t].x, o.x);
+              o.y = fmaf(ww, v[t].y, o.y);
+              o.z = fmaf(ww, v[t].z, o.z);
+              o.w = fmaf(ww, v[t].w, o.w);
+            }
+          }
+        }
+        l = warp_sum(l);
+      }
+      write_row(a, row0 + r, lane, M, l, o);
     }
   }
-  return true;
+}
+
+// Consumer side of a piece's end: wait until the merge warp has read the
+// previous piece's states (bounded), then the caller writes its state.
+__device__ __forceinline__ bool handoff_wait(const Smem& sm, uint32_t handed) {
+  return handed == 0 || mbar_wait_bounded(sm.mfree, (handed - 1) & 1u);
+}
+
+// After the caller's state is written: consumer 0 names the piece, every
+// consumer thread arrives.
+__device__ __forceinline__ void handoff_signal(const Smem& sm, int w, int lane, int item, int k) {
+  if (w == 0 && lane == 0) {
+    sm.minfo[0] = item;
+    sm.minfo[1] = k;
+  }
+  mbar_arrive(sm.mready);
 }
 
 // ------------------------------------------------------------------ f32 consumers
@@ -425,7 +519,6 @@ __device__ bool finish_piece(const FusedDecArgs& a, const Smem& sm, uint32_t& ph
 template <int R, int S>
 __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int lane) {
   constexpr Layout L = fused_layout<false, R, S>();
-  constexpr int NC = Cfg<false>::NC;
   const int ck = a.block_size < kCK ? a.block_size : kCK;
   const int kb = a.page_size < ck ? a.page_size : ck;
   const int lkb = __ffs(kb) - 1;                  // kb is a power of two
@@ -447,7 +540,7 @@ __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int l
     l_run[r] = 0.f;
     o[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  uint32_t xc = 0, phase = 0;
+  uint32_t xc = 0, handed = 0;
   for (;;) {
     const int s = static_cast<int>(xc % S);
     if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
@@ -455,7 +548,10 @@ __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int l
       return;
     }
     const StageHdr hd = sm.hdr[s];
-    if (hd.flags & kDone) return;
+    if (hd.flags & kDone) {
+      if (handoff_wait(sm, handed)) handoff_signal(sm, w, lane, -1, 0);
+      return;
+    }
     const unsigned char* kt = sm.base + s * L.stage;
     const unsigned char* vt = kt + L.tensor;
     // Q rows of the piece: row 4 r + quarter, chunks swizzled like K.
@@ -532,6 +628,10 @@ __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int l
     }
     mbar_arrive(sm.empty + s);
     if (hd.flags & kLast) {
+      if (!handoff_wait(sm, handed)) {
+        if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float lw = qd == 0 ? l_run[r] : 0.f;
@@ -544,10 +644,8 @@ __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int l
           sm.ml[w * R + r] = lw;
         }
       }
-      if (!finish_piece<NC, R>(a, sm, phase, hd.item, hd.k, w * 32 + lane)) {
-        if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
-        return;
-      }
+      handoff_signal(sm, w, lane, hd.item, hd.k);
+      ++handed;
     }
     ++xc;
   }
@@ -591,9 +689,8 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 
 template <int R, int S>
 __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int lane) {
-  static_assert(R == 8 || R == 16, "rows of the m16 tile");
+  static_assert(R == 16, "rows g and g + 8 of the m16 tile are both query rows");
   constexpr Layout L = fused_layout<true, R, S>();
-  constexpr int NC = Cfg<true>::NC;
   const int g = lane >> 2, c = lane & 3;          // fragment row (and + 8), column pair
   const int mi = lane >> 3, ri = lane & 7;        // ldmatrix matrix and row
   // K rows for S = Q K^T: matrices (keys 0-7 | 8-15) x (dims lo | hi 8 of 16).
@@ -615,7 +712,7 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
 #pragma unroll
     for (int e = 0; e < 4; ++e) qhi[ks][e] = qlo[ks][e] = 0u;
 
-  uint32_t xc = 0, phase = 0;
+  uint32_t xc = 0, handed = 0;
   for (;;) {
     const int s = static_cast<int>(xc % S);
     if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
@@ -623,7 +720,10 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
       return;
     }
     const StageHdr hd = sm.hdr[s];
-    if (hd.flags & kDone) return;
+    if (hd.flags & kDone) {
+      if (handoff_wait(sm, handed)) handoff_signal(sm, w, lane, -1, 0);
+      return;
+    }
     const uint32_t kt = smem_u32(sm.base + s * L.stage);
     const uint32_t vt = kt + L.tensor;
     if (hd.flags & kFirst) {
@@ -734,6 +834,10 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
     }
     mbar_arrive(sm.empty + s);
     if (hd.flags & kLast) {
+      if (!handoff_wait(sm, handed)) {
+        if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         float l = l_part[h2];
@@ -751,10 +855,161 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
           }
         }
       }
-      if (!finish_piece<NC, R>(a, sm, phase, hd.item, hd.k, w * 32 + lane)) {
+      handoff_signal(sm, w, lane, hd.item, hd.k);
+      ++handed;
+    }
+    ++xc;
+  }
+}
+
+// Up to 8 query rows (qhead <= 8): rows g + 8 of the m16 tile carry the bf16
+// remainders of rows g, for Q in S = Q K^T and for P in O += P V, so the
+// split costs no extra MMA; accumulator rows g and g + 8 are summed.
+template <int S>
+__device__ void consumer_bf16_packed(const FusedDecArgs& a, const Smem& sm, int w, int lane) {
+  constexpr int R = 8;
+  constexpr Layout L = fused_layout<true, R, S>();
+  const int g = lane >> 2, c = lane & 3;          // fragment row, column pair
+  const int mi = lane >> 3, ri = lane & 7;        // ldmatrix matrix and row
+  const uint32_t krow = static_cast<uint32_t>(16 * w + (mi >> 1) * 8 + ri) * 128u;
+  const uint32_t vrow = static_cast<uint32_t>(16 * w + (mi & 1) * 8 + ri) * 128u;
+  const float qscale = a.scale * kLog2e;
+
+  float m_run = -INFINITY;
+  float l_part = 0.f;
+  float o[16][4];           // [n-tile][row g: 0-1 | row g + 8 (remainder part): 2-3]
+  uint32_t qa[8][4];        // A fragments: high parts in rows g, remainders in rows g + 8
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qa[ks][e] = 0u;
+
+  uint32_t xc = 0, handed = 0;
+  for (;;) {
+    const int s = static_cast<int>(xc % S);
+    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
+      if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const StageHdr hd = sm.hdr[s];
+    if (hd.flags & kDone) {
+      if (handoff_wait(sm, handed)) handoff_signal(sm, w, lane, -1, 0);
+      return;
+    }
+    const uint32_t kt = smem_u32(sm.base + s * L.stage);
+    const uint32_t vt = kt + L.tensor;
+    if (hd.flags & kFirst) {
+      const float* qg = sm.qs + s * R * kD;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float2 v = make_float2(0.f, 0.f);
+          if (g < a.qhead) v = *reinterpret_cast<const float2*>(qg + g * kD + 16 * ks + 2 * c + 8 * half);
+          split2(v.x * qscale, v.y * qscale, qa[ks][2 * half], qa[ks][2 * half + 1]);
+        }
+      }
+      m_run = -INFINITY;
+      l_part = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+    }
+    const uint32_t mk = (w < 2 ? hd.mask_lo >> (16 * w) : hd.mask_hi >> (16 * (w - 2))) & 0xFFFFu;
+    if (mk) {
+      // ---- S = Q K^T for the warp's 16 keys: two chains (even / odd k-steps) ----
+      float sc[2][2];
+      {
+        float part[2][2][4];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) part[qq][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t chunk = static_cast<uint32_t>(((ks & 3) << 1) | (mi & 1));
+          uint32_t b[4];
+          ldsm_x4(kt + (ks >> 2) * (kCK * 128) + krow + ((chunk ^ ri) << 4), b);
+          mma16816(part[ks & 1][0], qa[ks], b[0], b[1]);
+          mma16816(part[ks & 1][1], qa[ks], b[2], b[3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            sc[nt][e] = (part[0][nt][e] + part[0][nt][e + 2]) + (part[1][nt][e] + part[1][nt][e + 2]);
+      }
+      // ---- online softmax of row g ----
+      float cm = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kk = 8 * nt + 2 * c + e;
+          sc[nt][e] = ((mk >> kk) & 1u) ? sc[nt][e] : -INFINITY;
+          cm = fmaxf(cm, sc[nt][e]);
+        }
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+      const float m_new = fmaxf(m_run, cm);          // finite: the warp has a key
+      const float alpha = exp2f(m_run - m_new);
+      float pv[2][2];
+      float lsum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pv[nt][e] = exp2f(sc[nt][e] - m_new);
+          lsum += pv[nt][e];
+        }
+      l_part = fmaf(l_part, alpha, lsum);
+      m_run = m_new;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][e] *= alpha;
+      }
+      uint32_t pa[4];
+      split2(pv[0][0], pv[0][1], pa[0], pa[1]);
+      split2(pv[1][0], pv[1][1], pa[2], pa[3]);
+      // ---- O += P V (16 n-tiles of 8 dims) ----
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        const uint32_t chunk = static_cast<uint32_t>(((np & 3) << 1) | (mi >> 1));
+        uint32_t b[4];
+        ldsm_x4_t(vt + (np >> 2) * (kCK * 128) + vrow + ((chunk ^ ri) << 4), b);
+        mma16816(o[2 * np], pa, b[0], b[1]);
+        mma16816(o[2 * np + 1], pa, b[2], b[3]);
+      }
+    }
+    mbar_arrive(sm.empty + s);
+    if (hd.flags & kLast) {
+      if (!handoff_wait(sm, handed)) {
         if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
         return;
       }
+      float l = l_part;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      float* dst = sm.mo + (w * R + g) * kD + 2 * c;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<float2*>(dst + 8 * nt) =
+            make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+      if (c == 0) {
+        sm.mm[w * R + g] = m_run;
+        sm.ml[w * R + g] = l;
+      }
+      handoff_signal(sm, w, lane, hd.item, hd.k);
+      ++handed;
     }
     ++xc;
   }
@@ -763,11 +1018,12 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
 // ------------------------------------------------------------------ kernel
 
 template <bool kBf16, int R, int S>
-__global__ void __launch_bounds__((2 + Cfg<kBf16>::NC) * 32, 1)
+__global__ void __launch_bounds__((2 + Cfg<kBf16>::NL + Cfg<kBf16>::NC) * 32, 1)
 fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
   extern __shared__ unsigned char smem_raw[];
   constexpr Layout L = fused_layout<kBf16, R, S>();
   constexpr int NC = Cfg<kBf16>::NC;
+  constexpr int NL = Cfg<kBf16>::NL;
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Smem sm;
@@ -782,8 +1038,9 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
   sm.empty = sm.full + S;
   sm.dfull = sm.empty + S;
   sm.dempty = sm.dfull + kDescs;
-  sm.merge = sm.dempty + kDescs;
-  sm.flag = reinterpret_cast<volatile int*>(base + L.flag);
+  sm.mready = sm.dempty + kDescs;
+  sm.mfree = sm.mready + 1;
+  sm.minfo = reinterpret_cast<volatile int*>(base + L.flag);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -793,9 +1050,10 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
     }
     for (int d = 0; d < kDescs; ++d) {
       mbar_init(sm.dfull + d, 32);
-      mbar_init(sm.dempty + d, 32);
+      mbar_init(sm.dempty + d, 32 * Cfg<kBf16>::NL);
     }
-    mbar_init(sm.merge, NC * 32);
+    mbar_init(sm.mready, NC * 32);
+    mbar_init(sm.mfree, 32);
     fence_mbar_init();
   }
   // Keys (and Q rows past qhead) that are never copied enter products that
@@ -805,15 +1063,20 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
   fence_proxy_async_smem();
   __syncthreads();
 
-  const int64_t n_pieces = a.tq * a.hkv * a.pieces;
+  const int64_t n_pieces = a.whole_items + (a.tq * a.hkv - a.whole_items) * a.pieces;
   if (warp == 0) {
     meta_warp(a, sm, n_pieces, lane);
-  } else if (warp == 1) {
-    load_warp<kBf16, R, S>(maps, a, sm, lane);
+  } else if (warp <= NL) {
+    load_warp<kBf16, R, S>(maps, a, sm, warp - 1, lane);
+  } else if (warp == NL + 1) {
+    merge_warp<NC, R>(a, sm, lane);
   } else if constexpr (kBf16) {
-    consumer_bf16<R, S>(a, sm, warp - 2, lane);
+    if constexpr (R == 8)
+      consumer_bf16_packed<S>(a, sm, warp - NL - 2, lane);
+    else
+      consumer_bf16<R, S>(a, sm, warp - NL - 2, lane);
   } else {
-    consumer_f32<R, S>(a, sm, warp - 2, lane);
+    consumer_f32<R, S>(a, sm, warp - NL - 2, lane);
   }
 }
 
@@ -871,6 +1134,7 @@ template <bool kBf16, int R, int S>
 cudaError_t launch_fused(const FusedDecArgs& a, cudaStream_t stream) {
   constexpr Layout L = fused_layout<kBf16, R, S>();
   constexpr int NC = Cfg<kBf16>::NC;
+  constexpr int NL = Cfg<kBf16>::NL;
   const size_t smem = L.total + 1024;
   if (smem > 227 * 1024) return cudaErrorNotSupported;
   const int ck = a.block_size < kCK ? a.block_size : kCK;
@@ -900,12 +1164,12 @@ cudaError_t launch_fused(const FusedDecArgs& a, cudaStream_t stream) {
   cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const int64_t n_pieces = a.tq * a.hkv * a.pieces;
+  const int64_t n_pieces = a.whole_items + (a.tq * a.hkv - a.whole_items) * a.pieces;
   int64_t grid = device_sm_count();
   if (grid > n_pieces) grid = n_pieces;
   if (grid < 1) return cudaSuccess;
   fused_dec_kernel<kBf16, R, S>
-      <<<static_cast<unsigned>(grid), (2 + NC) * 32, smem, stream>>>(maps, a);
+      <<<static_cast<unsigned>(grid), (2 + NL + NC) * 32, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -926,7 +1190,9 @@ bool fused_dec_supported(int head_dim, int block_size, int page_size, int qhead,
 cudaError_t launch_fused_dec(const FusedDecArgs& a, cudaStream_t stream) {
   if (!fused_dec_supported(kD, a.block_size, a.page_size, a.qhead, a.kv_bf16))
     return cudaErrorNotSupported;
-  if (a.ranks_per_piece < 1 || a.ranks_per_piece > kMaxEP || a.pieces < 1)
+  if (a.ranks_per_piece < 1 || a.ranks_per_piece > kMaxEP || a.pieces < 1 ||
+      static_cast<int64_t>(a.pieces) * a.ranks_per_piece < a.topk || a.whole_items < 0 ||
+      a.whole_items > a.tq * a.hkv || (a.whole_items > 0 && a.topk > kMaxEP))
     return cudaErrorInvalidValue;
   if (a.num_pages < 1 || a.num_pages * a.hkv * a.page_size > kFusedMaxRows)
     return cudaErrorNotSupported;

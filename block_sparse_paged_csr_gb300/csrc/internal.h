@@ -106,8 +106,10 @@ struct FusedDecArgs {
   const int32_t* inv;       // [hkv, tq, topk] of the built index
   int64_t tq;
   int32_t batch, hq, hkv, qhead, topk, block_size, page_size, pages_per_block, max_pages, msb;
-  int32_t pieces;           // pieces per (query, kv head)
-  int32_t ranks_per_piece;  // at most 32
+  int64_t whole_items;      // (query, kv head) pairs [0, whole_items): one piece of all
+                            // ranks each (topk <= 64); the rest: `pieces` pieces each
+  int32_t pieces;           // pieces per pair from whole_items on
+  int32_t ranks_per_piece;  // ranks of one of those pieces, at most 64
   float scale;
   int64_t* status;          // device status word
   uint32_t* item_cnt;       // [tq * hkv], zero on entry, left zero

@@ -324,9 +324,11 @@ sa_status sa_combine(const sa_index *idx, const float *o_partial, const float *m
  * run as one kernel that keeps each query's partials on chip: every work
  * unit of such a batch carries edges of a single query, so the combine only
  * ever merges a (query, kv head)'s own units.  The index is still built in
- * full.  The kernel splits each (query, kv head)'s ranks into pieces of
- * split_edges ranks (at most 32; 0 = chosen from the SM count) and merges the
- * pieces through rows of the partial buffers, whose content afterwards is
+ * full.  With split_edges = 0 each (query, kv head) is one piece of work
+ * (topk <= 64), except that the pairs of the last, partial round over the
+ * SMs are cut into pieces to fill the SMs; split_edges > 0 cuts every pair
+ * into pieces of split_edges ranks (at most 64).  Pieces of one pair are
+ * merged through rows of the partial buffers, whose content afterwards is
  * unspecified.  out and lse equal those of the unfused path up to rounding.
  */
 sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,

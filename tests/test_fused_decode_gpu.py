@@ -66,18 +66,32 @@ def test_fused_decode_shapes(dt, bs, ps, qhead, split):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_fused_decode_many_ranks_and_no_used(dt):
-    """topk above 32 (several pieces even at the largest piece size) and
+    """topk above 64 (several pieces even at the largest piece size) and
     used_kv_lens = None (every block of the table row is addressable)."""
     w = decode_case(dt, 64, 16, 4, seed=91, topk=20, pass_used=False)
-    w.selected = np.concatenate([w.selected, w.selected[:, :, :20]], axis=2)   # topk 40
-    w.topk = 40
+    w.selected = np.concatenate([w.selected] * 4, axis=2)        # topk 80, blocks repeated
+    w.topk = 80
     t = _gpu.device_workload(w)
-    for split in (0, 32):
+    for split in (0, 64, 7):
         out, lse, idx, _ = _gpu.run_attention(w, t, split_edges=split)
         ref_out, ref_lse, ref_idx = oracle_out(w, split)
         _gpu.compare_index(idx.to_host(), ref_idx)
         assert _gpu.row_error(out.cpu().numpy(), ref_out) <= _gpu.TOL_F32
         _gpu.compare_lse(lse.cpu().numpy(), ref_lse, _gpu.TOL_F32)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_fused_decode_more_pairs_than_sms(dt):
+    """Enough (query, kv head) pairs for whole-pair pieces on every SM plus a
+    last, partial round whose pairs are cut into pieces."""
+    w = decode_case(dt, 64, 16, 4, seed=23, batch=101)
+    assert w.tq * w.hkv > 152
+    t = _gpu.device_workload(w)
+    out, lse, idx, _ = _gpu.run_attention(w, t)
+    ref_out, ref_lse, ref_idx = oracle_out(w, 0)
+    _gpu.compare_index(idx.to_host(), ref_idx)
+    assert _gpu.row_error(out.cpu().numpy(), ref_out) <= _gpu.TOL_F32
+    _gpu.compare_lse(lse.cpu().numpy(), ref_lse, _gpu.TOL_F32)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
