@@ -3,25 +3,36 @@
 // alice-llm's sparse_attention) for work units with many gathered rows
 // (chunked prefill, skewed selections).
 //
-// A CTA (4 warps, thread t <-> accumulator row t; two CTAs per SM) takes
-// (kv head, block) units round-robin, so the CTAs running together work on
-// neighbouring blocks of one (kv head, sequence) and share its Q rows in L2.
-// For each unit it converts the block's K and V rows (fetched through the
-// block table, f32 or bf16) to bf16 once, in shared memory laid out for the
-// tensor cores: K as [keys x 128] and V transposed as [128 x keys], both
-// K-major with the 128-byte swizzle.  For every tile of up to 128 of the
-// unit's rows (edge x GQA lane) it then
-//   1. gathers the rows' Q (f32 -> bf16, same layout),
-//   2. issues S = Q K^T (M=128, N=block, K=128) into TMEM,
-//   3. reads S back one row per thread (tcgen05.ld), masks (block length,
-//      absent pages, right-aligned causal limit), computes m, p = exp(s - m)
-//      and l, and stores p as bf16 over the (now unused) Q tile,
-//   4. issues O = P V (M=128, N=128, K=block) into TMEM,
-//   5. reads O back one row per thread and writes the unnormalised partial
-//      row with its m and l.
-// One thread issues the MMAs; tcgen05.commit signals an mbarrier.  Operands
-// are rounded to bf16 (tolerance class of the tensor-core path); S, O and
-// the softmax statistics stay in f32.
+// A persistent CTA per SM takes (kv head, block) units round-robin, so the
+// SMs working at the same time cover neighbouring blocks of one (kv head,
+// sequence) and share its Q rows in L2.  A unit's rows (edge x GQA lane) go
+// through 128-row tiles.  Warp roles, coupled by mbarriers:
+//   warps 1-7  loaders: per unit, the block's K and V rows (through the
+//              block table, f32 or bf16) converted to bf16 once, K as
+//              [keys x 128] and V transposed as [128 x keys], K-major with the
+//              128-byte swizzle (two unit buffers, so the next unit loads
+//              while this one computes); per tile, the rows' Q (f32 -> bf16,
+//              same layout) and each row's causal limit (two or three tile
+//              buffers, so the gathers' latency stays off the path);
+//   warp 0     one thread issues S = Q K^T (M=128, N=block, K=128) into TMEM
+//              and, once the softmax has turned S into P, O = P V (M=128,
+//              N=128, K=block; P from TMEM); tcgen05.commit signals the
+//              mbarriers;
+//   warps 8-15 softmax and epilogue, two warpgroups taking alternate tiles
+//              (and the matching S / O buffer), thread t <-> row t of the
+//              tile (TMEM lane t): S back
+//              with tcgen05.ld, masks (block length, absent pages,
+//              right-aligned causal limit), m, p = exp(s - m), l, and P as
+//              bf16 pairs back into S's TMEM columns (tcgen05.st), where the
+//              second MMA takes it as its A operand; the tile buffer thus
+//              holds Q only and frees as soon as S is done; then the
+//              previous tile's O back from
+//              TMEM and its unnormalised partial row (staged through shared
+//              memory for whole-line stores), m and l to memory.
+// S and O are double-buffered in TMEM (512 columns), so S of tile t + 1 and
+// the epilogue of tile t - 1 overlap the softmax of tile t.  Operands are
+// rounded to bf16 (tolerance class of the tensor-core path); S, O and the
+// softmax statistics stay in f32.
 #include <cstdint>
 
 #include "internal.h"
@@ -33,10 +44,10 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;            // rows per MMA tile
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;   // MMA warp, 7 loader warps, 2 x 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kTmemCols = 256;  // S at column 0 (<= 128 columns), O at column 128
+constexpr uint32_t kTmemCols = 512;  // S[2] at columns 0 / 128, O[2] at 256 / 384
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -69,6 +80,31 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM, row i in lane i, two bf16 per column) x B (smem)^T.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -134,24 +170,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-struct TcPlan {
-  size_t k_off, v_off, qp_off, pos_off, off_off, total;
-};
-
-// Shared memory: K [BS][128] and V^T [128][BS] (bf16, swizzled), one tile
-// buffer used first for Q [128][128] and then for P [128][BS], per-key
-// positions and row offsets.
-__host__ __device__ inline TcPlan tc_plan(int bs) {
-  TcPlan p{};
-  p.k_off = 1024;                                   // [0, 1024): barrier, TMEM slot, unit bases
-  p.v_off = p.k_off + static_cast<size_t>(bs) * kD * 2;
-  p.qp_off = p.v_off + static_cast<size_t>(kD) * bs * 2;
-  p.pos_off = p.qp_off + static_cast<size_t>(kM) * kD * 2;
-  p.off_off = p.pos_off + static_cast<size_t>(bs) * 4;
-  p.total = p.off_off + static_cast<size_t>(bs) * 8 + 1024;   // + alignment slack
-  return p;
-}
-
+// Four K/V elements (f32 or bf16) as packed bf16 (round to nearest even).
 template <bool kBf16>
 __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off) {
   if constexpr (kBf16) {
@@ -162,96 +181,133 @@ __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off
   }
 }
 
-template <bool kBf16>
-__device__ __forceinline__ float ld_kv1(const void* pages, int64_t elem_off) {
-  if constexpr (kBf16) {
-    return bf16_to_f32(__ldg(static_cast<const uint16_t*>(pages) + elem_off));
-  } else {
-    return __ldg(static_cast<const float*>(pages) + elem_off);
-  }
+constexpr int kLoaders = 7;          // loader warps 1..7
+constexpr int kLoadThreads = 32 * kLoaders;
+constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 19
+constexpr int kQBatch = 10;          // Q rows in flight per loader lane
+
+template <int BS> struct TcCfg {
+  static constexpr int KVB = 2;                   // unit buffers (K, V^T)
+  static constexpr int NX = BS == 128 ? 2 : 3;    // tile buffers (Q, then P)
+};
+constexpr int kMaxNX = 3;
+
+struct UnitInfo {
+  int32_t rows;         // edges x qhead of the unit (0: skip)
+  int32_t h;
+  int64_t prow0;        // first partial row of the unit
+  int64_t e0;           // first edge of the unit (absolute)
+  int64_t q0, qo, lk;   // the sequence's first query, query count, KV length
+  int64_t bstart;       // position of the block's first key
+};
+
+// Shared memory: KVB unit buffers (K, V^T), NX tile buffers (Q), key
+// positions and unit info per unit buffer, key offsets of the unit being
+// loaded, the epilogue's staging tiles, barriers, the TMEM address and
+// per-head unit bases.
+struct TcPlan {
+  size_t kv_bytes;      // one unit buffer: K [BS][128] + V^T [128][BS] bf16
+  size_t kv, x, kpos, info, koff, stage, bars, misc, total;
+};
+
+__host__ __device__ inline TcPlan tc_plan(int bs) {
+  const int kvb = 2;
+  const int nx = bs == 128 ? 2 : 3;
+  TcPlan p{};
+  p.kv_bytes = static_cast<size_t>(bs) * kD * 2 * 2;
+  p.kv = 0;                                               // 1024-aligned
+  p.x = p.kv + kvb * p.kv_bytes;                          // [nx] tiles of 32 KB
+  p.kpos = p.x + nx * static_cast<size_t>(kM) * kD * 2;   // int32 [kvb][BS]
+  p.info = p.kpos + kvb * static_cast<size_t>(bs) * 4;    // UnitInfo [kvb]
+  p.koff = p.info + kvb * sizeof(UnitInfo);               // int64 [BS]
+  p.stage = p.koff + static_cast<size_t>(bs) * 8;         // f32 [8 warps][32 rows][16], swizzled
+  p.bars = p.stage + 8 * 32 * 16 * 4;                     // uint64 [32]
+  p.misc = p.bars + 32 * 8;                               // TMEM slot, unit bases [201]
+  p.total = p.misc + 16 + 201 * 4 + 1024;                 // + alignment slack
+  return p;
 }
 
-template <int BS, bool kBf16>
-__global__ void __launch_bounds__(kThreads)
-forward_tc_kernel(ForwardArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  // 1024-byte alignment for the swizzled tiles.
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const TcPlan plan = tc_plan(BS);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 16);
-  int32_t* unit_base = reinterpret_cast<int32_t*>(smem + 64);       // [hkv+1], hkv <= 200
-  unsigned char* ks = smem + plan.k_off;     // K   [BS rows][128] bf16, K-major SW128
-  unsigned char* vs = smem + plan.v_off;     // V^T [128 rows][BS] bf16, K-major SW128
-  unsigned char* qp = smem + plan.qp_off;    // Q [128][128], later P [128][BS] bf16
-  int32_t* kpos = reinterpret_cast<int32_t*>(smem + plan.pos_off);   // [BS] position or -1
-  int64_t* koff = reinterpret_cast<int64_t*>(smem + plan.off_off);   // [BS] row offset or -1
+struct TcBars {
+  uint64_t *kv_full, *kv_empty;        // [KVB]
+  uint64_t *x_full, *x_empty;          // [NX]
+  uint64_t *s_full, *s_free;           // [2] TMEM S buffers
+  uint64_t *p_full, *o_full, *o_free;  // [2]
+  uint64_t* done;
+};
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+// OR of `pred` over the loader warps (named barrier 1); also a barrier.
+__device__ __forceinline__ bool loaders_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "n"(kLoadThreads)
+      : "memory");
+  return r != 0;
+}
+
+// Unit u's head h and compact slot j from the per-head unit bases.
+__device__ __forceinline__ void unit_head(const int32_t* unit_base, int hkv, int64_t u, int& h,
+                                          int& j) {
+  h = 0;
+  while (h + 1 < hkv && unit_base[h + 1] <= u) ++h;
+  j = static_cast<int>(u - unit_base[h]);
+}
+
+// ------------------------------------------------------------------ loaders
+
+template <int BS, bool kBf16>
+__device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
+                          const TcBars& B, const int32_t* unit_base, int64_t n_units, int lw,
+                          int lane) {
+  constexpr int KVB = TcCfg<BS>::KVB;
+  constexpr int kNX = TcCfg<BS>::NX;
+  const int lt = lw * 32 + lane;
   const int qhead = a.qhead;
   const int ps = a.page_size;
   int64_t* status = a.totals + 3;
-  const float qscale = a.scale * kLog2e;
-
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    int32_t acc = 0;
-    for (int hh = 0; hh < a.hkv; ++hh) {
-      unit_base[hh] = acc;
-      acc += a.num_sel[hh];
-    }
-    unit_base[a.hkv] = acc;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem;            // S: columns [0, BS)
-  const uint32_t t_o = tmem + 128;      // O: columns [128, 256)
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const int64_t n_units = unit_base[a.hkv];
-  uint32_t phase = 0;
-  bool ok = true;
-
-  // Units round-robin over CTAs: CTAs running at the same time work on
-  // neighbouring blocks of one (kv head, sequence), whose Q rows stay in L2.
-  for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    int h = 0;
-    while (h + 1 < a.hkv && unit_base[h + 1] <= u) ++h;
-    const int j = static_cast<int>(u - unit_base[h]);
+  int64_t* koff = reinterpret_cast<int64_t*>(smem + P.koff);
+  uint32_t U = 0, T = 0;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+    const int kvb = static_cast<int>(U % KVB);
+    unsigned char* ks = smem + P.kv + kvb * P.kv_bytes;
+    unsigned char* vs = ks + static_cast<size_t>(BS) * kD * 2;
+    int32_t* kpos = reinterpret_cast<int32_t*>(smem + P.kpos) + kvb * BS;
+    UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + P.info) + kvb;
+    int h, j;
+    unit_head(unit_base, a.hkv, u, h, j);
     const int raw = a.sel_slots[static_cast<int64_t>(h) * a.nbs + j];
     const int64_t ebase = a.edge_head_base[h];
     const int64_t e0 = ebase + a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j];
     const int64_t e1 = ebase + a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j + 1];
-    if (raw < 0 || raw >= a.nbs || e1 < e0) {
-      if (tid == 0) report(status, SA_ERR_SHAPE);
-      continue;
-    }
-    const int b = raw / a.msb;
-    const int blk = raw - b * a.msb;
+    const bool bad = raw < 0 || raw >= a.nbs || e1 < e0;
+    if (bad && lt == 0) report(status, SA_ERR_SHAPE);
+    const int b = bad ? 0 : raw / a.msb;
+    const int blk = bad ? 0 : raw - b * a.msb;
     const int64_t lk = a.used ? max(a.used[b], 0) : static_cast<int64_t>(a.msb) * BS;
     const int64_t bstart = static_cast<int64_t>(blk) * BS;
     const int64_t bend = min(bstart + BS, lk);
     const int64_t q0 = a.cu[b];
     const int64_t qo = a.cu[b + 1] - q0;
+    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
 
-    // ---- K and V^T of the unit ---------------------------------------------
-    __syncthreads();   // the previous unit's MMAs were waited for: K / V are free
+    bool got = U < static_cast<uint32_t>(KVB) ||
+               mbar_wait_bounded(B.kv_empty + kvb, ((U / KVB) - 1) & 1u);
+    if (loaders_or(!got)) {
+      if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    // ---- the unit's keys: position (or -1) and source offset ----------------
     const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
                         static_cast<int64_t>(blk) * a.pages_per_block;
-    for (int jj = tid; jj < BS; jj += kThreads) {
+    for (int jj = lt; jj < BS; jj += kLoadThreads) {
       const int64_t pos = bstart + jj;
       int32_t live = -1;
       int64_t off = -1;
-      if (pos < bend) {
+      if (!bad && pos < bend) {
         const int pid = bt[jj / ps];
         if (pid >= a.num_pages) report(status, SA_ERR_SHAPE);
         if (pid >= 0 && pid < a.num_pages) {
@@ -262,24 +318,31 @@ forward_tc_kernel(ForwardArgs a) {
       kpos[jj] = live;
       koff[jj] = off;
     }
-    __syncthreads();
-    // K rows: warp-cooperative (lane = 4 dims), all of a warp's rows in flight.
+    loaders_or(false);   // koff visible to all loaders
+    // K rows: lane = 4 dims, ten of a warp's rows in flight at a time.
     {
-      uint2 kr[BS / 4];
+      constexpr int kRows = (BS + kLoaders - 1) / kLoaders;
 #pragma unroll
-      for (int q = 0; q < BS / 4; ++q) {
-        const int64_t off = koff[warp + 4 * q];
-        kr[q] = off >= 0 ? ld_kv4_bf16<kBf16>(a.k_pages, off + 4 * lane) : make_uint2(0u, 0u);
+      for (int q0 = 0; q0 < kRows; q0 += 10) {
+        uint2 kr[10];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          const int64_t off = q0 + q < kRows && r < BS ? koff[r] : -1;
+          kr[q] = off >= 0 ? ld_kv4_bf16<kBf16>(a.k_pages, off + 4 * lane) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          if (q0 + q < kRows && r < BS)
+            *reinterpret_cast<uint2*>(ks + sw128_offset(BS, r, 4 * lane)) = kr[q];
+        }
       }
-#pragma unroll
-      for (int q = 0; q < BS / 4; ++q)
-        *reinterpret_cast<uint2*>(ks + sw128_offset(BS, warp + 4 * q, 4 * lane)) = kr[q];
     }
     // V^T: a warp takes 8 keys at a time; lane l loads dims 4l..4l+3 of each
-    // (coalesced rows), then writes, for each of its 4 dims d, the 8 keys as
-    // one 16-byte chunk of row d.  The order of the 4 dims is rotated by lane
-    // so the 8 lanes of a store phase hit 8 different bank groups.
-    for (int kc = warp; kc < BS / 8; kc += kThreads / 32) {
+    // key, then writes, for each of its 4 dims d, the 8 keys as one 16-byte
+    // chunk of row d (dim order rotated by lane against bank conflicts).
+    for (int kc = lw; kc < BS / 8; kc += kLoaders) {
       float4 v[8];
 #pragma unroll
       for (int uu = 0; uu < 8; ++uu) {
@@ -306,173 +369,406 @@ forward_tc_kernel(ForwardArgs a) {
         packed.y = pack_bf16x2_rn(c8[2], c8[3]);
         packed.z = pack_bf16x2_rn(c8[4], c8[5]);
         packed.w = pack_bf16x2_rn(c8[6], c8[7]);
-        const int d = 4 * lane + comp;
-        *reinterpret_cast<uint4*>(vs + sw128_offset(kD, d, kc * 8)) = packed;
+        *reinterpret_cast<uint4*>(vs + sw128_offset(kD, 4 * lane + comp, kc * 8)) = packed;
       }
     }
+    if (lt == 0) {
+      info->rows = rows;
+      info->h = h;
+      info->prow0 = e0 * qhead;
+      info->e0 = e0;
+      info->q0 = q0;
+      info->qo = qo;
+      info->lk = lk;
+      info->bstart = bstart;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(B.kv_full + kvb);
 
-    // Keys present in the block (position inside the length, page not absent).
+    // ---- tiles: Q rows and causal limits ------------------------------------
+    // Warp lw gathers rows lw + kLoaders q of a tile: lane q holds row q's Q
+    // source (found for the next tile while this tile's rows are in flight),
+    // then the rows are loaded ten at a time (lane = 4 dims of a row).
+    auto row_source = [&](int rt) -> int64_t {
+      const int r = lw + lane * kLoaders;
+      if (lane < kRowsPerLoader && r < kM && rt + r < rows) {
+        const int row = rt + r;
+        const int64_t qi = a.edges[2 * (e0 + row / qhead)];
+        return (qi * a.hq + static_cast<int64_t>(h) * qhead + row % qhead) * kD;
+      }
+      return -1;
+    };
+    int64_t my_src = row_source(0);
+    for (int rt = 0; rt < rows; rt += kM, ++T) {
+      const int xb = static_cast<int>(T % kNX);
+      got = T < static_cast<uint32_t>(kNX) ||
+            mbar_wait_bounded(B.x_empty + xb, ((T / kNX) - 1) & 1u);
+      if (loaders_or(!got)) {
+        if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      unsigned char* xq = smem + P.x + static_cast<size_t>(xb) * kM * kD * 2;
+      int64_t nxt_src = -1;
+#pragma unroll
+      for (int q0 = 0; q0 < kRowsPerLoader; q0 += kQBatch) {
+        float4 v[kQBatch];
+#pragma unroll
+        for (int q = 0; q < kQBatch; ++q) {
+          const int64_t src = __shfl_sync(0xffffffffu, my_src, (q0 + q) & 31);
+          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q0 + q < kRowsPerLoader && src >= 0)
+            v[q] = __ldg(reinterpret_cast<const float4*>(a.q + src) + lane);
+        }
+        if (q0 == 0 && rt + kM < rows) nxt_src = row_source(rt + kM);
+#pragma unroll
+        for (int q = 0; q < kQBatch; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          if (q0 + q < kRowsPerLoader && r < kM)
+            *reinterpret_cast<uint2*>(xq + sw128_offset(kM, r, 4 * lane)) =
+                make_uint2(pack_bf16x2_rn(v[q].x, v[q].y), pack_bf16x2_rn(v[q].z, v[q].w));
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(B.x_full + xb);
+      my_src = nxt_src;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issue
+
+template <int BS>
+__device__ bool tc_issue_o(unsigned char* smem, const TcPlan& P, const TcBars& B, uint32_t tmem,
+                           int kvb, uint32_t T) {
+  const int sb = static_cast<int>(T & 1u);
+  if (!mbar_wait_bounded(B.p_full + sb, (T >> 1) & 1u)) return false;
+  if (T >= 2 && !mbar_wait_bounded(B.o_free + sb, ((T >> 1) - 1) & 1u)) return false;
+  tc_fence_after();
+  const uint32_t v_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes + static_cast<size_t>(BS) * kD * 2);
+  const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs) over S's columns
+  const uint32_t t_o = tmem + 256 + 128 * sb;
+#pragma unroll
+  for (int st = 0; st < BS / 16; ++st) {
+    const uint32_t panel = st >> 2;
+    const uint32_t kb = (st & 3) * 32;
+    mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc(v_addr + panel * kD * 128 + kb),
+                idesc_bf16(kM, kD), st > 0);
+  }
+  mma_commit(B.o_full + sb);
+  mma_commit(B.s_free + sb);                     // P read: the S / P columns are free
+  return true;
+}
+
+template <int BS>
+__device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
+                       const TcBars& B, uint32_t tmem, int64_t n_units) {
+  constexpr int KVB = TcCfg<BS>::KVB;
+  constexpr int kNX = TcCfg<BS>::NX;
+  int64_t* status = a.totals + 3;
+  uint32_t U = 0, T = 0;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+    const int kvb = static_cast<int>(U % KVB);
+    if (!mbar_wait_bounded(B.kv_full + kvb, (U / KVB) & 1u)) {
+      report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const UnitInfo* info = reinterpret_cast<const UnitInfo*>(smem + P.info) + kvb;
+    const int rows = info->rows;
+    const uint32_t k_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes);
+    tc_fence_after();
+    const int tiles = (rows + kM - 1) / kM;
+    for (int tt = 0; tt < tiles; ++tt, ++T) {
+      const int sb = static_cast<int>(T & 1u);
+      const int xb = static_cast<int>(T % kNX);
+      if (!mbar_wait_bounded(B.x_full + xb, (T / kNX) & 1u) ||
+          (T >= 2 && !mbar_wait_bounded(B.s_free + sb, ((T >> 1) - 1) & 1u))) {
+        report(status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(smem + P.x + static_cast<size_t>(xb) * kM * kD * 2);
+      const uint32_t t_s = tmem + 128 * sb;
+#pragma unroll
+      for (int st = 0; st < kD / 16; ++st) {
+        const uint32_t panel = st >> 2;
+        const uint32_t kb = (st & 3) * 32;
+        mma_bf16(t_s, sw128_desc(q_addr + panel * kM * 128 + kb),
+                 sw128_desc(k_addr + panel * BS * 128 + kb), idesc_bf16(kM, BS), st > 0);
+      }
+      mma_commit(B.s_full + sb);
+      mma_commit(B.x_empty + xb);                // Q read: the tile buffer is free
+      if (tt > 0 && !tc_issue_o<BS>(smem, P, B, tmem, kvb, T - 1)) {
+        report(status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+    }
+    if (tiles > 0 && !tc_issue_o<BS>(smem, P, B, tmem, kvb, T - 1)) {
+      report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    mma_commit(B.kv_empty + kvb);
+  }
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+
+// Softmax warpgroup g (0 or 1) takes the tiles whose running index has
+// parity g, and with them TMEM buffers S[g], O[g].
+template <int BS>
+__device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
+                           const TcBars& B, uint32_t tmem, int64_t n_units, int warp, int lane) {
+  const uint32_t g = static_cast<uint32_t>((warp - 1 - kLoaders) >> 2);
+  constexpr int KVB = TcCfg<BS>::KVB;
+  int64_t* status = a.totals + 3;
+  const int row = (warp & 3) * 32 + lane;               // TMEM lane = tile row
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const float qscale = a.scale * kLog2e;
+  float* wst = reinterpret_cast<float*>(smem + P.stage) + (g * 4 + (warp & 3)) * 32 * 16;
+  // The previous tile's row, stored after this tile's softmax.
+  bool prev = false;
+  uint32_t prevT = 0;
+  int64_t prev_prow = -1;
+  float prev_m = -INFINITY, prev_l = 0.f;
+
+  auto epilogue = [&](uint32_t Tp, int64_t prow, float m2, float l) -> bool {
+    const int sb = static_cast<int>(Tp & 1u);
+    const bool got = mbar_wait_bounded(B.o_full + sb, (Tp >> 1) & 1u);
+    if (!__all_sync(0xffffffffu, got)) return false;
+    tc_fence_after();
+    const uint32_t t_o = tmem + 256 + 128 * sb + lane_base;
+    // 16 columns at a time: each thread puts 16 of its row's values into the
+    // warp's staging tile (16-byte chunk i of row r at i ^ ((r >> 1) & 3), so
+    // 8 consecutive rows hit 8 different bank groups), then the warp writes
+    // 8 rows x 64 bytes per store instruction.  Valid rows are a prefix of
+    // the tile, so a warp with a valid row has lane 0 valid.
+    const int64_t prow0 = __shfl_sync(0xffffffffu, prow, 0);
+    const unsigned live = __ballot_sync(0xffffffffu, prow >= 0);
+#pragma unroll 1
+    for (int c = 0; c < kD / 32; ++c) {
+      float v[32];
+      tmem_ld32(t_o + c * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<float4*>(wst + lane * 16)[i ^ ((lane >> 1) & 3)] =
+              make_float4(v[16 * hf + 4 * i], v[16 * hf + 4 * i + 1], v[16 * hf + 4 * i + 2],
+                          v[16 * hf + 4 * i + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = 8 * k + (lane >> 2);
+          const int ch = lane & 3;
+          if ((live >> r) & 1u) {
+            const float4 val = reinterpret_cast<const float4*>(wst + r * 16)[ch ^ ((r >> 1) & 3)];
+            reinterpret_cast<float4*>(a.o_partial + (prow0 + r) * kD + c * 32 + 16 * hf)[ch] = val;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(B.o_free + sb);
+    if (prow >= 0) {
+      a.m_partial[prow] = m2 == -INFINITY ? -INFINITY : m2 * kLn2;
+      a.l_partial[prow] = l;
+    }
+    return true;
+  };
+
+  uint32_t U = 0, T = 0;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+    const int kvb = static_cast<int>(U % KVB);
+    const bool gk = mbar_wait_bounded(B.kv_full + kvb, (U / KVB) & 1u);
+    if (!__all_sync(0xffffffffu, gk)) {
+      if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const UnitInfo info = reinterpret_cast<const UnitInfo*>(smem + P.info)[kvb];
+    const int32_t* kpos = reinterpret_cast<const int32_t*>(smem + P.kpos) + kvb * BS;
     uint32_t vmask[BS / 32];
 #pragma unroll
     for (int c = 0; c < BS / 32; ++c) vmask[c] = __ballot_sync(0xffffffffu, kpos[c * 32 + lane] >= 0);
-
-    const int rows = static_cast<int>((e1 - e0) * qhead);
-    for (int rt = 0; rt < rows && ok; rt += kM) {
-      const int nrows = min(kM, rows - rt);
-      // ---- Q tile: lane l of warp w owns row 32w + l's query --------------------
-      {
-        const int r = warp * 32 + lane;
-        int64_t my_src = -1;
-        if (r < nrows) {
-          const int row = rt + r;
-          const int64_t qi = a.edges[2 * (e0 + row / qhead)];
-          my_src = (qi * a.hq + static_cast<int64_t>(h) * qhead + row % qhead) * kD;
-        }
-        // All 32 row loads in flight before any is used.
-        float4 v[32];
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr) {
-          const int64_t src = __shfl_sync(0xffffffffu, my_src, rr);
-          v[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (src >= 0) v[rr] = __ldg(reinterpret_cast<const float4*>(a.q + src) + lane);
-        }
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr) {
-          const uint2 packed =
-              make_uint2(pack_bf16x2_rn(v[rr].x, v[rr].y), pack_bf16x2_rn(v[rr].z, v[rr].w));
-          *reinterpret_cast<uint2*>(qp + sw128_offset(kM, warp * 32 + rr, 4 * lane)) = packed;
+    mbar_arrive(B.kv_empty + kvb);                      // info and keys read
+    const int tiles = (info.rows + kM - 1) / kM;
+    for (int tt = 0; tt < tiles; ++tt, ++T) {
+      if ((T & 1u) != g) continue;                      // the other warpgroup's tile
+      // This warpgroup's previous tile's partial row first: its O buffer is
+      // then free by the time this tile's P is ready.
+      if (prev && !epilogue(prevT, prev_prow, prev_m, prev_l)) {
+        if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      prev = false;
+      const int sb = static_cast<int>(T & 1u);
+      // This row's last live key of the block under the causal limit (its
+      // query read before S is awaited).
+      const int nrows = min(kM, info.rows - tt * kM);
+      int jlim = -1;
+      if (row < nrows) {
+        jlim = BS - 1;
+        if (a.causal) {
+          const int rr = tt * kM + row;
+          const int64_t qi = a.edges[2 * (info.e0 + rr / a.qhead)];
+          const int64_t ql = qi - info.q0;
+          const int64_t lim = info.lk >= info.qo ? info.lk - info.qo + ql : ql;
+          const int64_t rel = lim - info.bstart;
+          jlim = rel < -1 ? -1 : (rel > BS - 1 ? BS - 1 : static_cast<int>(rel));
         }
       }
-      // This thread's row: last live key of the block under the causal limit.
-      const bool row_ok = tid < nrows;
-      int jlim = row_ok ? BS - 1 : -1;
-      if (row_ok && a.causal) {
-        const int row = rt + tid;
-        const int64_t qi = a.edges[2 * (e0 + row / qhead)];
-        const int64_t ql = qi - q0;
-        const int64_t lim = lk >= qo ? lk - qo + ql : ql;
-        const int64_t rel = lim - bstart;
-        jlim = rel < -1 ? -1 : (rel > BS - 1 ? BS - 1 : static_cast<int>(rel));
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-
-      // ---- S = Q K^T ------------------------------------------------------------
-      if (tid == 0) {
-        const uint32_t q_addr = smem_u32(qp);
-        const uint32_t k_addr = smem_u32(ks);
-#pragma unroll
-        for (int st = 0; st < kD / 16; ++st) {
-          const uint32_t panel = st >> 2;
-          const uint32_t kb = (st & 3) * 32;
-          mma_bf16(t_s, sw128_desc(q_addr + panel * kM * 128 + kb),
-                   sw128_desc(k_addr + panel * BS * 128 + kb), idesc_bf16(kM, BS), st > 0);
-        }
-        mma_commit(bar);
-      }
-      bool got = mbar_wait_bounded(bar, phase);
-      phase ^= 1u;
-      if (__syncthreads_or(!got)) {
-        if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
-        ok = false;
-        break;
+      const bool got = mbar_wait_bounded(B.s_full + sb, (T >> 1) & 1u);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+        return;
       }
       tc_fence_after();
-
-      // ---- softmax of this thread's row; P overwrites the Q tile -----------------
+      const uint32_t t_s = tmem + 128 * sb + lane_base;
+      // pass 1: the row maximum over live keys
       float m2 = -INFINITY;
-      float sc[BS];
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < BS / 32; ++c) {
         float v[32];
-        tmem_ld32(t_s + lane_base + c * 32, v);
+        tmem_ld32(t_s + c * 32, v);
         tmem_ld_wait();
-        // live keys of this chunk for this row: present and at or before jlim
-        const int cut = jlim - c * 32;        // keys i <= cut are inside the limit
+        const int cut = jlim - c * 32;
         const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
         const uint32_t live = vmask[c] & inside;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sc[c * 32 + i] = ((live >> i) & 1u) ? v[i] * qscale : -INFINITY;
-          m2 = fmaxf(m2, sc[c * 32 + i]);
-        }
+        for (int i = 0; i < 32; ++i)
+          if ((live >> i) & 1u) m2 = fmaxf(m2, v[i] * qscale);
       }
+      // pass 2: p = exp(s - m), l, and P as bf16 pairs into the S columns
+      // already read (chunk c's 16 columns lie at or before S chunk c).
       const float msub = m2 == -INFINITY ? 0.f : m2;
       float l = 0.f;
-#pragma unroll
-      for (int j0 = 0; j0 < BS; j0 += 8) {
-        float p8[8];
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          p8[uu] = exp2f(sc[j0 + uu] - msub);   // exp2(-inf) = 0
-          l += p8[uu];
-        }
-        uint4 packed;
-        packed.x = pack_bf16x2_rn(p8[0], p8[1]);
-        packed.y = pack_bf16x2_rn(p8[2], p8[3]);
-        packed.z = pack_bf16x2_rn(p8[4], p8[5]);
-        packed.w = pack_bf16x2_rn(p8[6], p8[7]);
-        *reinterpret_cast<uint4*>(qp + sw128_offset(kM, tid, j0)) = packed;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-
-      // ---- O = P V ----------------------------------------------------------------
-      if (tid == 0) {
-        const uint32_t p_addr = smem_u32(qp);
-        const uint32_t v_addr = smem_u32(vs);
-#pragma unroll
-        for (int st = 0; st < BS / 16; ++st) {
-          const uint32_t panel = st >> 2;
-          const uint32_t kb = (st & 3) * 32;
-          mma_bf16(t_o, sw128_desc(p_addr + panel * kM * 128 + kb),
-                   sw128_desc(v_addr + panel * kD * 128 + kb), idesc_bf16(kM, kD), st > 0);
-        }
-        mma_commit(bar);
-      }
-      got = mbar_wait_bounded(bar, phase);
-      phase ^= 1u;
-      if (__syncthreads_or(!got)) {
-        if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-
-      // ---- epilogue: this thread's partial row -------------------------------------
-      const int64_t prow = e0 * qhead + rt + tid;
-#pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
+#pragma unroll 1
+      for (int c = 0; c < BS / 32; ++c) {
         float v[32];
-        tmem_ld32(t_o + lane_base + c * 32, v);
+        tmem_ld32(t_s + c * 32, v);
         tmem_ld_wait();
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(a.o_partial + prow * kD + c * 32);
+        const int cut = jlim - c * 32;
+        const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
+        const uint32_t live = vmask[c] & inside;
+        uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const int i = 2 * i2;
+          const float p0 = ((live >> i) & 1u) ? exp2f(fmaf(v[i], qscale, -msub)) : 0.f;
+          const float p1 = ((live >> (i + 1)) & 1u) ? exp2f(fmaf(v[i + 1], qscale, -msub)) : 0.f;
+          l += p0 + p1;
+          pk[i2] = pack_bf16x2_rn(p0, p1);
         }
+        tmem_st16(t_s + c * 16, pk);
       }
-      if (row_ok) {
-        a.m_partial[prow] = m2 == -INFINITY ? -INFINITY : m2 * kLn2;
-        a.l_partial[prow] = l;
-      }
+      tmem_st_wait();
       tc_fence_before();
-      __syncthreads();   // S / O / the tile buffer are free for the next tile
-      tc_fence_after();
+      mbar_arrive(B.p_full + sb);
+      prev = true;
+      prevT = T;
+      prev_prow = row < nrows ? info.prow0 + static_cast<int64_t>(tt) * kM + row : -1;
+      prev_m = m2;
+      prev_l = l;
     }
+    // The unit's last tile before the next unit's keys.
+    if (prev && !epilogue(prevT, prev_prow, prev_m, prev_l)) {
+      if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    prev = false;
   }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int BS, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+forward_tc_kernel(ForwardArgs a) {
+  constexpr int KVB = TcCfg<BS>::KVB;
+  constexpr int kNX = TcCfg<BS>::NX;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const TcPlan P = tc_plan(BS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  TcBars B;
+  B.kv_full = bars;
+  B.kv_empty = bars + 2;
+  B.x_full = bars + 4;
+  B.x_empty = bars + 4 + kMaxNX;
+  B.s_full = bars + 4 + 2 * kMaxNX;
+  B.s_free = B.s_full + 2;
+  B.p_full = B.s_full + 4;
+  B.o_full = B.s_full + 6;
+  B.o_free = B.s_full + 8;
+  B.done = B.s_full + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc);
+  int32_t* unit_base = reinterpret_cast<int32_t*>(smem + P.misc + 16);   // [hkv + 1]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int i = 0; i < KVB; ++i) {
+      mbar_init(B.kv_full + i, kLoadThreads);
+      // freed by the unit's last MMA and by both softmax warpgroups (which
+      // read the unit's info and keys even when a one-tile unit gives them
+      // no tile)
+      mbar_init(B.kv_empty + i, 1 + 2 * kM);
+    }
+    for (int i = 0; i < kNX; ++i) {
+      mbar_init(B.x_full + i, kLoadThreads);
+      mbar_init(B.x_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B.s_full + i, 1);
+      mbar_init(B.s_free + i, 1);
+      mbar_init(B.p_full + i, kM);
+      mbar_init(B.o_full + i, 1);
+      mbar_init(B.o_free + i, kM);
+    }
+    mbar_init(B.done, 1);
+    fence_mbar_init();
+    int32_t acc = 0;
+    for (int hh = 0; hh < a.hkv; ++hh) {
+      unit_base[hh] = acc;
+      acc += a.num_sel[hh];
+    }
+    unit_base[a.hkv] = acc;
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int64_t n_units = unit_base[a.hkv];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc_mma<BS>(a, smem, P, B, tmem, n_units);
+      // Every MMA issued has completed before TMEM is released.
+      mma_commit(B.done);
+      if (!mbar_wait_bounded(B.done, 0)) report(a.totals + 3, SA_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp <= kLoaders) {
+    tc_loader<BS, kBf16>(a, smem, P, B, unit_base, n_units, warp - 1, lane);
+  } else {
+    tc_softmax<BS>(a, smem, P, B, tmem, n_units, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int BS, bool kBf16>
 cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
   const TcPlan p = tc_plan(BS);
+  if (p.total > 227 * 1024) return cudaErrorNotSupported;
   const void* fn = reinterpret_cast<const void*>(forward_tc_kernel<BS, kBf16>);
   cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
@@ -480,11 +776,8 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
   err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  // Two CTAs per SM when their shared memory fits (two CTAs x 256 TMEM
-  // columns fill an SM's TMEM); the occupancy query is not used because it
-  // reported one CTA where two fit.
-  const int per_sm = 2 * (p.total + 1024) <= 228 * 1024 ? 2 : 1;
-  int64_t grid = static_cast<int64_t>(device_sm_count()) * per_sm;
+  // One CTA per SM: it holds all 512 TMEM columns.
+  int64_t grid = device_sm_count();
   if (grid > a.max_splits) grid = a.max_splits;
   if (grid < 1) grid = 1;
   forward_tc_kernel<BS, kBf16><<<static_cast<unsigned>(grid), kThreads, p.total, stream>>>(a);
