@@ -7,7 +7,7 @@
 // SMs working at the same time cover neighbouring blocks of one (kv head,
 // sequence) and share its Q rows in L2.  A unit's rows (edge x GQA lane) go
 // through 128-row tiles.  Warp roles, coupled by mbarriers:
-//   warps 1-7  loaders: per unit, the block's K and V rows (through the
+//   warps 1-15 loaders: per unit, the block's K and V rows (through the
 //              block table, f32 or bf16) converted to bf16 once, K as
 //              [keys x 128] and V transposed as [128 x keys], K-major with the
 //              128-byte swizzle (two unit buffers, so the next unit loads
@@ -18,7 +18,7 @@
 //              and, once the softmax has turned S into P, O = P V (M=128,
 //              N=128, K=block; P from TMEM); tcgen05.commit signals the
 //              mbarriers;
-//   warps 8-15 softmax and epilogue, two warpgroups taking alternate tiles
+//   warps 16-23 softmax and epilogue, two warpgroups taking alternate tiles
 //              (and the matching S / O buffer), thread t <-> row t of the
 //              tile (TMEM lane t): S back
 //              with tcgen05.ld, masks (block length, absent pages,
@@ -44,7 +44,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;            // rows per MMA tile
-constexpr int kThreads = 512;   // MMA warp, 7 loader warps, 2 x 4 softmax warps
+constexpr int kThreads = 768;   // MMA warp, 15 loader warps, 2 x 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // S[2] at columns 0 / 128, O[2] at 256 / 384
@@ -181,10 +181,10 @@ __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off
   }
 }
 
-constexpr int kLoaders = 7;          // loader warps 1..7
+constexpr int kLoaders = 15;         // loader warps 1..15
 constexpr int kLoadThreads = 32 * kLoaders;
-constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 19
-constexpr int kQBatch = 10;          // Q rows in flight per loader lane
+constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 9
+constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
 
 template <int BS> struct TcCfg {
   static constexpr int KVB = 2;                   // unit buffers (K, V^T)
@@ -210,22 +210,28 @@ struct TcPlan {
   size_t kv, x, kpos, info, koff, stage, bars, misc, total;
 };
 
+__host__ __device__ constexpr size_t tc_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Every region starts on a 128-byte boundary (the swizzled tiles on 1024):
+// float4 staging, int64 offsets and mbarriers all need their alignment
+// whatever the sizes of the regions before them.
 __host__ __device__ inline TcPlan tc_plan(int bs) {
-  const int kvb = 2;
-  const int nx = bs == 128 ? 2 : 3;
+  const int kvb = bs == 128 ? TcCfg<128>::KVB : TcCfg<64>::KVB;
+  const int nx = bs == 128 ? TcCfg<128>::NX : TcCfg<64>::NX;
   TcPlan p{};
   p.kv_bytes = static_cast<size_t>(bs) * kD * 2 * 2;
-  p.kv = 0;                                               // 1024-aligned
-  p.x = p.kv + kvb * p.kv_bytes;                          // [nx] tiles of 32 KB
-  p.kpos = p.x + nx * static_cast<size_t>(kM) * kD * 2;   // int32 [kvb][BS]
-  p.info = p.kpos + kvb * static_cast<size_t>(bs) * 4;    // UnitInfo [kvb]
-  p.koff = p.info + kvb * sizeof(UnitInfo);               // int64 [BS]
-  p.stage = p.koff + static_cast<size_t>(bs) * 8;         // f32 [8 warps][32 rows][16], swizzled
-  p.bars = p.stage + 8 * 32 * 16 * 4;                     // uint64 [32]
-  p.misc = p.bars + 32 * 8;                               // TMEM slot, unit bases [201]
-  p.total = p.misc + 16 + 201 * 4 + 1024;                 // + alignment slack
+  p.kv = 0;                                                             // 1024-aligned
+  p.x = p.kv + kvb * p.kv_bytes;                                        // [nx] tiles of 32 KB
+  p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * 2, 128);     // int32 [kvb][BS]
+  p.info = tc_up(p.kpos + kvb * static_cast<size_t>(bs) * 4, 128);      // UnitInfo [kvb]
+  p.koff = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // int64 [BS]
+  p.stage = tc_up(p.koff + static_cast<size_t>(bs) * 8, 128);           // f32 [8][32][16]
+  p.bars = tc_up(p.stage + 8 * 32 * 16 * 4, 128);                       // uint64 [32]
+  p.misc = tc_up(p.bars + 32 * 8, 128);                                 // TMEM slot, unit bases
+  p.total = p.misc + 16 + 201 * 4 + 1024;                               // + alignment slack
   return p;
 }
+static_assert(sizeof(UnitInfo) % 8 == 0, "UnitInfo holds int64 fields");
 
 struct TcBars {
   uint64_t *kv_full, *kv_empty;        // [KVB]
@@ -624,7 +630,8 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
       }
       tc_fence_after();
       const uint32_t t_s = tmem + 128 * sb + lane_base;
-      // pass 1: the row maximum over live keys
+      // pass 1: the row maximum over live keys (fully live chunks, the common
+      // case, without per-key masks)
       float m2 = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < BS / 32; ++c) {
@@ -634,9 +641,14 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
         const int cut = jlim - c * 32;
         const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
         const uint32_t live = vmask[c] & inside;
+        if (live == 0xffffffffu) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if ((live >> i) & 1u) m2 = fmaxf(m2, v[i] * qscale);
+          for (int i = 0; i < 32; ++i) m2 = fmaxf(m2, v[i] * qscale);
+        } else if (live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if ((live >> i) & 1u) m2 = fmaxf(m2, v[i] * qscale);
+        }
       }
       // pass 2: p = exp(s - m), l, and P as bf16 pairs into the S columns
       // already read (chunk c's 16 columns lie at or before S chunk c).
@@ -651,13 +663,23 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
         const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
         const uint32_t live = vmask[c] & inside;
         uint32_t pk[16];
+        if (live == 0xffffffffu) {
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-          const int i = 2 * i2;
-          const float p0 = ((live >> i) & 1u) ? exp2f(fmaf(v[i], qscale, -msub)) : 0.f;
-          const float p1 = ((live >> (i + 1)) & 1u) ? exp2f(fmaf(v[i + 1], qscale, -msub)) : 0.f;
-          l += p0 + p1;
-          pk[i2] = pack_bf16x2_rn(p0, p1);
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const float p0 = exp2f(fmaf(v[2 * i2], qscale, -msub));
+            const float p1 = exp2f(fmaf(v[2 * i2 + 1], qscale, -msub));
+            l += p0 + p1;
+            pk[i2] = pack_bf16x2_rn(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int i = 2 * i2;
+            const float p0 = ((live >> i) & 1u) ? exp2f(fmaf(v[i], qscale, -msub)) : 0.f;
+            const float p1 = ((live >> (i + 1)) & 1u) ? exp2f(fmaf(v[i + 1], qscale, -msub)) : 0.f;
+            l += p0 + p1;
+            pk[i2] = pack_bf16x2_rn(p0, p1);
+          }
         }
         tmem_st16(t_s + c * 16, pk);
       }
