@@ -218,6 +218,32 @@ class ClockSampler:
 # --------------------------------------------------------------------------- ours
 
 
+def aggregate_ranks(elapsed_s, e2e_per_rank, world, device):
+    """Whole-job figures of a replicated run: the slowest rank's elapsed time
+    (every rank did the same amount of work) and the end-to-end throughput as
+    world x the slowest rank's.  world = 1 returns the inputs unchanged."""
+    if world <= 1:
+        return elapsed_s, e2e_per_rank
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([elapsed_s], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed = float(t.item())
+    e2e_total = None
+    if e2e_per_rank is not None:
+        t = torch.tensor([e2e_per_rank], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        e2e_total = float(t.item()) * world
+    return elapsed, e2e_total
+
+
+def job_throughput(queries_per_step, steps, world, elapsed_s):
+    """Queries per second of the whole job: every rank ran `steps` steps of
+    `queries_per_step` queries; the job took the slowest rank's time."""
+    return world * queries_per_step * steps / elapsed_s
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -356,16 +382,10 @@ def run_ours(args, rank, world, local_rank):
                "steps": n_e2e}
 
     # ---- aggregate over ranks -----------------------------------------------
-    elapsed_s = total_ms / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_s = float(t.item())
-        if e2e is not None:
-            t = torch.tensor([e2e["value"]], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MIN)
-            e2e["value"] = float(t.item()) * world
+    elapsed_s, e2e_total = aggregate_ranks(total_ms / 1e3, e2e["value"] if e2e else None, world,
+                                           dev)
+    if e2e is not None:
+        e2e["value"] = e2e_total
     if rank != 0:
         return None
 
@@ -376,7 +396,7 @@ def run_ours(args, rank, world, local_rank):
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
     fwd_file = fwd_kernel.replace("_kernel", ".cu")
     traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", ""))
-    value = world * w.tq * args.steps / elapsed_s
+    value = job_throughput(w.tq, args.steps, world, elapsed_s)
     dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
