@@ -66,6 +66,10 @@ def make_workload(name: str, seed: int):
         w = inputs.gqa_decode(seed, kv_min=4096, kv_max=6144)
         w.name = name
         return w
+    if name == "chunked_prefill_ncu":
+        w = inputs.chunked_prefill(seed, batch=1)
+        w.name = name
+        return w
     if name == "long_decode_ncu":
         w = inputs.long_decode(seed, batch=128, kv_min=8192, kv_max=12288)
         w.name = name
