@@ -393,8 +393,9 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
 
     // ---- tiles: Q rows and causal limits ------------------------------------
     // Warp lw gathers rows lw + kLoaders q of a tile: lane q holds row q's Q
-    // source (found for the next tile while this tile's rows are in flight),
-    // then the rows are loaded ten at a time (lane = 4 dims of a row).
+    // source (found, and prefetched into L2, for the next tile while this
+    // tile's rows are in flight), then the rows are loaded (lane = 4 dims of
+    // a row).
     auto row_source = [&](int rt) -> int64_t {
       const int r = lw + lane * kLoaders;
       if (lane < kRowsPerLoader && r < kM && rt + r < rows) {
@@ -425,7 +426,14 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
           if (q0 + q < kRowsPerLoader && src >= 0)
             v[q] = __ldg(reinterpret_cast<const float4*>(a.q + src) + lane);
         }
-        if (q0 == 0 && rt + kM < rows) nxt_src = row_source(rt + kM);
+        if (q0 == 0 && rt + kM < rows) {
+          nxt_src = row_source(rt + kM);
+          // the next tile's rows start for L2 now; their loads come a tile later
+          if (nxt_src >= 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.q + nxt_src),
+                         "r"(static_cast<uint32_t>(kD * 4))
+                         : "memory");
+        }
 #pragma unroll
         for (int q = 0; q < kQBatch; ++q) {
           const int r = lw + (q0 + q) * kLoaders;
