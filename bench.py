@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partials", default="f32", choices=["f32", "bf16"],
+                    help="o partial storage: f32 (the pages' layout) or the opt-in bf16")
     return ap.parse_args()
 
 
@@ -80,11 +82,12 @@ def make_workload(name: str, seed: int):
 # --------------------------------------------------------------------------- accounting
 
 
-def algorithmic_bytes(w, fused=False) -> dict:
+def algorithmic_bytes(w, fused=False, o_bytes=4) -> dict:
     """Bytes the KV-outer method must move, from the workload's own index
     inputs: each kept (kv head, block) loads its live keys' K and V once, Q is
     read once, the partials are written by the forward and read by the
-    combine, the output is written once.  On the fused decode path the
+    combine (o at o_bytes per value: 4, or 2 for the opt-in bf16 o partials;
+    m and l at 4), the output is written once.  On the fused decode path the
     partials stay on chip, so its one kernel ("forward") moves K, V, Q, the
     index's inv rows and the output."""
     elt = 2 if w.kv_dtype == "bf16" else 4
@@ -113,7 +116,7 @@ def algorithmic_bytes(w, fused=False) -> dict:
                 flops += 4 * w.head_dim * nk * n_e * w.qhead        # upper bound (no causal cut)
     kv = 2 * kv_keys * w.head_dim * elt
     q = w.tq * w.hq * w.head_dim * 4
-    parts = edges * w.qhead * (w.head_dim + 2) * 4
+    parts = edges * w.qhead * (w.head_dim * o_bytes + 2 * 4)
     out = w.tq * w.hq * w.head_dim * 4
     inv = w.hkv * w.tq * w.topk * 4
     if fused:
@@ -261,7 +264,7 @@ def run_ours(args, rank, world, local_rank):
     fwd_kernel = sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq,
                                              w.head_dim, w.block_size, w.page_size, w.kv_dtype)
     fused = fwd_kernel == "fused_dec_kernel"
-    acct = algorithmic_bytes(w, fused)
+    acct = algorithmic_bytes(w, fused, o_bytes=2 if args.partials == "bf16" else 4)
 
     q, k, v = inputs.device_tensors(w, dev)
     sel = torch.from_numpy(w.selected).to(dev)
@@ -276,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
         return sa.sa_attention(q, k, v, sel, cu_host, cu, used, bt, w.hq, w.hkv, w.head_dim,
                                w.block_size, w.page_size, w.softmax_scale, w.causal,
                                split_edges=split, index=index, partials=partials, out=out,
-                               lse=lse)
+                               lse=lse, partial_dtype=args.partials if partials is None else None)
 
     out, lse, index, partials = step()
     torch.cuda.synchronize(dev)
@@ -399,7 +402,8 @@ def run_ours(args, rank, world, local_rank):
     step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
     fwd_file = fwd_kernel.replace("_kernel", ".cu")
-    traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", ""))
+    traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", "") +
+                          ("_bf16p" if args.partials == "bf16" and not fused else ""))
     value = job_throughput(w.tq, args.steps, world, elapsed_s)
     dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"
     return {
@@ -411,6 +415,7 @@ def run_ours(args, rank, world, local_rank):
             "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size,
             "topk": w.topk, "max_pages": w.max_pages, "num_pages": w.num_pages,
             "kv_dtype": w.kv_dtype, "causal": w.causal, "split_edges": split,
+            "o_partials": args.partials,
             "l2": "flushed before every timed step (512 MiB write, outside the step events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "selected_kv_gbs": kv_gbs,

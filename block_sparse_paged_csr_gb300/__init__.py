@@ -249,6 +249,27 @@ def sa_attention_kernel_name(cu_seqlens_q_host, num_pages, hkv, hq, head_dim, bl
     return None if name is None else name.decode()
 
 
+_PARTIAL_DTYPES = {"f32": (torch.float32, 0), "bf16": (torch.bfloat16, 1)}
+
+
+def _partial_dtype(partial_dtype, o_partial):
+    """(torch dtype, sa_dtype code) of the o partials: from ``o_partial`` when
+    given (float32 or bfloat16), else ``partial_dtype`` ("f32" default, or
+    "bf16": 16-bit o partials, an opt-in the pages do not have)."""
+    if o_partial is not None:
+        for name, (dt, code) in _PARTIAL_DTYPES.items():
+            if o_partial.dtype == dt:
+                if partial_dtype not in (None, name):
+                    raise ValueError(f"o_partial is {o_partial.dtype}, partial_dtype {partial_dtype}")
+                return dt, code
+        raise TypeError(f"o_partial must be float32 or bfloat16, got {o_partial.dtype}")
+    if partial_dtype is None:
+        partial_dtype = "f32"
+    if partial_dtype not in _PARTIAL_DTYPES:
+        raise ValueError(f"partial_dtype must be 'f32' or 'bf16', got {partial_dtype!r}")
+    return _PARTIAL_DTYPES[partial_dtype]
+
+
 def partial_rows(index: Index, hq: int) -> int:
     """Row capacity of the partial buffers: tq * hkv * topk * qhead."""
     c = index.c
@@ -257,9 +278,10 @@ def partial_rows(index: Index, hq: int) -> int:
 
 def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, used_kv_lens, hq,
                hkv, head_dim, block_size, page_size, softmax_scale, causal, o_partial=None,
-               m_partial=None, l_partial=None, path=PATH_AUTO, stream=None):
+               m_partial=None, l_partial=None, path=PATH_AUTO, stream=None, partial_dtype=None):
     """Step 2.  Returns (o_partial, m_partial, l_partial); the first
-    totals[0] * qhead rows are valid."""
+    totals[0] * qhead rows are valid.  ``partial_dtype="bf16"`` (or a
+    bfloat16 ``o_partial``) stores o in bf16 (sa_forward_ex)."""
     _require(q, torch.float32, "q")
     dev = q.device
     kvd = _kv_dtype(k_pages)
@@ -272,41 +294,53 @@ def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, us
     page_elems = hkv * page_size * head_dim
     num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
     rows = partial_rows(index, hq) if hkv > 0 and hq % max(hkv, 1) == 0 else 1
+    odt, ocode = _partial_dtype(partial_dtype, o_partial)
     if o_partial is None:
-        o_partial = torch.empty((rows, head_dim), dtype=torch.float32, device=dev)
+        o_partial = torch.empty((rows, head_dim), dtype=odt, device=dev)
     if m_partial is None:
         m_partial = torch.empty(rows, dtype=torch.float32, device=dev)
     if l_partial is None:
         l_partial = torch.empty(rows, dtype=torch.float32, device=dev)
-    _check(_native.load().sa_forward(
-        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(index.c),
-        _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), hq, hkv, head_dim,
-        block_size, page_size, softmax_scale, int(bool(causal)), _ptr(o_partial),
-        _ptr(m_partial), _ptr(l_partial), path, _stream(stream, dev)), "sa_forward")
+    L = _native.load()
+    head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(index.c),
+            _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), hq, hkv, head_dim,
+            block_size, page_size, softmax_scale, int(bool(causal)))
+    tail = (_ptr(o_partial), _ptr(m_partial), _ptr(l_partial), path, _stream(stream, dev))
+    if ocode:
+        _check(L.sa_forward_ex(*head, ocode, *tail), "sa_forward_ex")
+    else:
+        _check(L.sa_forward(*head, *tail), "sa_forward")
     return o_partial, m_partial, l_partial
 
 
 def sa_combine(index: Index, o_partial, m_partial, l_partial, hq, head_dim, out=None, lse=None,
                with_lse=True, stream=None):
-    """Step 3.  Returns (out [tq, hq, d], lse [tq, hq] or None)."""
+    """Step 3.  Returns (out [tq, hq, d], lse [tq, hq] or None).  A bfloat16
+    ``o_partial`` is read as 16-bit o partials (sa_combine_ex)."""
     dev = o_partial.device
     tq = index.c.tq
+    _, ocode = _partial_dtype(None, o_partial)
     if out is None:
         out = torch.empty((tq, hq, head_dim), dtype=torch.float32, device=dev)
     if lse is None and with_lse:
         lse = torch.empty((tq, hq), dtype=torch.float32, device=dev)
-    _check(_native.load().sa_combine(ctypes.byref(index.c), _ptr(o_partial), _ptr(m_partial),
-                                     _ptr(l_partial), hq, head_dim, _ptr(out), _ptr(lse),
-                                     _stream(stream, dev)), "sa_combine")
+    L = _native.load()
+    tail = (_ptr(o_partial), _ptr(m_partial), _ptr(l_partial), hq, head_dim, _ptr(out), _ptr(lse),
+            _stream(stream, dev))
+    if ocode:
+        _check(L.sa_combine_ex(ctypes.byref(index.c), ocode, *tail), "sa_combine_ex")
+    else:
+        _check(L.sa_combine(ctypes.byref(index.c), *tail), "sa_combine")
     return out, lse
 
 
 def sa_forward_combine(q, k_pages, v_pages, index: Index, selected, cu_seqlens_q_host,
                        cu_seqlens_q, used_kv_lens, block_tables, hq, head_dim, block_size,
                        page_size, softmax_scale, causal, split_edges=0, partials=None, out=None,
-                       lse=None, with_lse=True, path=PATH_AUTO, stream=None):
+                       lse=None, with_lse=True, path=PATH_AUTO, stream=None, partial_dtype=None):
     """Steps 2 and 3 on a built index (the fused decode kernel where it
-    applies).  Returns (out, lse, (o, m, l))."""
+    applies).  Returns (out, lse, (o, m, l)).  ``partial_dtype="bf16"`` (or a
+    bfloat16 o in ``partials``): 16-bit o partials."""
     _require(q, torch.float32, "q")
     dev = q.device
     kvd = _kv_dtype(k_pages)
@@ -314,8 +348,9 @@ def sa_forward_combine(q, k_pages, v_pages, index: Index, selected, cu_seqlens_q
     hkv = c.hkv
     cu_h = _host_i64(cu_seqlens_q_host)
     rows = partial_rows(index, hq) if hkv > 0 and hq % max(hkv, 1) == 0 else 1
+    odt, ocode = _partial_dtype(partial_dtype, None if partials is None else partials[0])
     if partials is None:
-        partials = (torch.empty((rows, head_dim), dtype=torch.float32, device=dev),
+        partials = (torch.empty((rows, head_dim), dtype=odt, device=dev),
                     torch.empty(rows, dtype=torch.float32, device=dev),
                     torch.empty(rows, dtype=torch.float32, device=dev))
     if out is None:
@@ -325,21 +360,27 @@ def sa_forward_combine(q, k_pages, v_pages, index: Index, selected, cu_seqlens_q
     page_elems = hkv * page_size * head_dim
     num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
     o, m, l = partials
-    _check(_native.load().sa_forward_combine(
-        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(c), _ptr(selected),
-        cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), _ptr(used_kv_lens),
-        _ptr(block_tables), hq, head_dim, block_size, page_size, softmax_scale,
-        int(bool(causal)), split_edges, _ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path,
-        _stream(stream, dev)), "sa_forward_combine")
+    L = _native.load()
+    head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(c),
+            _ptr(selected), cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q),
+            _ptr(used_kv_lens), _ptr(block_tables), hq, head_dim, block_size, page_size,
+            softmax_scale, int(bool(causal)), split_edges)
+    tail = (_ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path, _stream(stream, dev))
+    if ocode:
+        _check(L.sa_forward_combine_ex(*head, ocode, *tail), "sa_forward_combine_ex")
+    else:
+        _check(L.sa_forward_combine(*head, *tail), "sa_forward_combine")
     return out, lse, partials
 
 
 def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens,
                  block_tables, hq, hkv, head_dim, block_size, page_size, softmax_scale, causal,
                  split_edges=0, index: Index | None = None, partials=None, out=None, lse=None,
-                 with_lse=True, path=PATH_AUTO, stream=None):
+                 with_lse=True, path=PATH_AUTO, stream=None, partial_dtype=None):
     """Steps 1-3 in one call.  Returns (out, lse, index, (o, m, l)).  Pass
-    ``index`` / ``partials`` / ``out`` back in to reuse their memory."""
+    ``index`` / ``partials`` / ``out`` back in to reuse their memory.
+    ``partial_dtype="bf16"`` (or a bfloat16 o in ``partials``): 16-bit o
+    partials (sa_attention_ex)."""
     _require(q, torch.float32, "q")
     dev = q.device
     kvd = _kv_dtype(k_pages)
@@ -351,8 +392,9 @@ def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q,
         index = allocate_index(tq, hkv_s, topk, max(batch, 1), max_pages, block_size, page_size,
                                dev)
     rows = max(tq * hkv_s * topk * (hq // max(hkv_s, 1)), 1)
+    odt, ocode = _partial_dtype(partial_dtype, None if partials is None else partials[0])
     if partials is None:
-        partials = (torch.empty((rows, head_dim), dtype=torch.float32, device=dev),
+        partials = (torch.empty((rows, head_dim), dtype=odt, device=dev),
                     torch.empty(rows, dtype=torch.float32, device=dev),
                     torch.empty(rows, dtype=torch.float32, device=dev))
     if out is None:
@@ -362,12 +404,16 @@ def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q,
     page_elems = hkv * page_size * head_dim
     num_pages = k_pages.numel() // page_elems if page_elems > 0 else 0
     o, m, l = partials
-    _check(_native.load().sa_attention(
-        _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, _ptr(selected), tq, topk,
-        cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), batch, _ptr(used_kv_lens),
-        _ptr(block_tables), max_pages, hq, hkv, head_dim, block_size, page_size, softmax_scale,
-        int(bool(causal)), split_edges, ctypes.byref(index.c), _ptr(o), _ptr(m), _ptr(l),
-        _ptr(out), _ptr(lse), path, _stream(stream, dev)), "sa_attention")
+    L = _native.load()
+    head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, _ptr(selected), tq, topk,
+            cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), batch, _ptr(used_kv_lens),
+            _ptr(block_tables), max_pages, hq, hkv, head_dim, block_size, page_size,
+            softmax_scale, int(bool(causal)), split_edges, ctypes.byref(index.c))
+    tail = (_ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path, _stream(stream, dev))
+    if ocode:
+        _check(L.sa_attention_ex(*head, ocode, *tail), "sa_attention_ex")
+    else:
+        _check(L.sa_attention(*head, *tail), "sa_attention")
     return out, lse, index, partials
 
 

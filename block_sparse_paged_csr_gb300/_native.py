@@ -19,8 +19,10 @@ PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL, PATH_FUSED_
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",
-           "sa_build_index_no_alloc", "sa_forward", "sa_forward_combine", "sa_forward_kernel_name",
-           "sa_attention_kernel_name", "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status")
+           "sa_build_index_no_alloc", "sa_forward", "sa_forward_ex", "sa_forward_combine",
+           "sa_forward_combine_ex", "sa_forward_kernel_name", "sa_attention_kernel_name",
+           "sa_combine", "sa_combine_ex", "sa_attention", "sa_attention_ex", "sa_get_status",
+           "sa_clear_status")
 
 
 class SaIndex(ctypes.Structure):
@@ -85,19 +87,32 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_forward.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, i32, i32, i32,
                                i32, i32, f32, i32, p, p, p, st, p]
     lib.sa_forward.restype = st
+    lib.sa_forward_ex.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, i32, i32,
+                                  i32, i32, i32, f32, i32, st, p, p, p, st, p]
+    lib.sa_forward_ex.restype = st
     lib.sa_forward_combine.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, p, p,
                                        i32, i32, i32, i32, f32, i32, i32, p, p, p, p, p, st, p]
     lib.sa_forward_combine.restype = st
+    lib.sa_forward_combine_ex.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, p,
+                                          p, i32, i32, i32, i32, f32, i32, i32, st, p, p, p, p,
+                                          p, st, p]
+    lib.sa_forward_combine_ex.restype = st
     lib.sa_forward_kernel_name.argtypes = [i64, i32, i32, i32, i32, i32, i32, st, st]
     lib.sa_forward_kernel_name.restype = ctypes.c_char_p
     lib.sa_attention_kernel_name.argtypes = [i64, i32, p, i64, i32, i32, i32, i32, i32, st, st]
     lib.sa_attention_kernel_name.restype = ctypes.c_char_p
     lib.sa_combine.argtypes = [ctypes.POINTER(SaIndex), p, p, p, i32, i32, p, p, p]
     lib.sa_combine.restype = st
+    lib.sa_combine_ex.argtypes = [ctypes.POINTER(SaIndex), st, p, p, p, i32, i32, p, p, p]
+    lib.sa_combine_ex.restype = st
     lib.sa_attention.argtypes = [p, p, p, i64, st, p, i64, i32, p, p, i32, p, p, i32, i32, i32,
                                  i32, i32, i32, f32, i32, i32, ctypes.POINTER(SaIndex), p, p, p,
                                  p, p, st, p]
     lib.sa_attention.restype = st
+    lib.sa_attention_ex.argtypes = [p, p, p, i64, st, p, i64, i32, p, p, i32, p, p, i32, i32,
+                                    i32, i32, i32, i32, f32, i32, i32, ctypes.POINTER(SaIndex),
+                                    st, p, p, p, p, p, st, p]
+    lib.sa_attention_ex.restype = st
     lib.sa_get_status.argtypes = [ctypes.POINTER(SaIndex), p]
     lib.sa_get_status.restype = st
     lib.sa_clear_status.argtypes = [ctypes.POINTER(SaIndex), p]

@@ -226,12 +226,13 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, int64_t num_pages,
-                     sa_dtype kv_dtype, const sa_index* idx, const int32_t* block_tables,
-                     const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, int32_t hq,
-                     int32_t hkv, int32_t head_dim, int32_t block_size, int32_t page_size,
-                     float softmax_scale, int32_t causal, float* o_partial, float* m_partial,
-                     float* l_partial, sa_path path, void* stream) {
+sa_status sa_forward_ex(const float* q, const void* k_pages, const void* v_pages,
+                        int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                        const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                        const int32_t* used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
+                        int32_t block_size, int32_t page_size, float softmax_scale,
+                        int32_t causal, sa_dtype partial_dtype, void* o_partial,
+                        float* m_partial, float* l_partial, sa_path path, void* stream) {
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return SA_ERR_BLOCK_PAGE;
@@ -241,6 +242,8 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
     return SA_ERR_SHAPE;
   if (num_pages < 0) return SA_ERR_SHAPE;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
+  if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
+    return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   if (path == SA_PATH_FUSED_DECODE) return SA_ERR_UNSUPPORTED;   // writes no partials
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
@@ -285,6 +288,7 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   a.totals = idx->totals;
   a.max_splits = idx->tq * idx->hkv * static_cast<int64_t>(idx->topk);
   a.o_partial = o_partial;
+  a.o_bf16 = partial_dtype == SA_DTYPE_BF16 ? 1 : 0;
   a.m_partial = m_partial;
   a.l_partial = l_partial;
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
@@ -298,6 +302,17 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
   }
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, int64_t num_pages,
+                     sa_dtype kv_dtype, const sa_index* idx, const int32_t* block_tables,
+                     const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, int32_t hq,
+                     int32_t hkv, int32_t head_dim, int32_t block_size, int32_t page_size,
+                     float softmax_scale, int32_t causal, float* o_partial, float* m_partial,
+                     float* l_partial, sa_path path, void* stream) {
+  return sa_forward_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables, cu_seqlens_q,
+                       used_kv_lens, hq, hkv, head_dim, block_size, page_size, softmax_scale,
+                       causal, SA_DTYPE_F32, o_partial, m_partial, l_partial, path, stream);
 }
 
 const char* sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_t hkv,
@@ -330,10 +345,12 @@ const char* sa_attention_kernel_name(int64_t tq, int32_t batch, const int64_t* c
                                 path);
 }
 
-sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m_partial,
-                     const float* l_partial, int32_t hq, int32_t head_dim, float* out, float* lse,
-                     void* stream) {
+sa_status sa_combine_ex(const sa_index* idx, sa_dtype partial_dtype, const void* o_partial,
+                        const float* m_partial, const float* l_partial, int32_t hq,
+                        int32_t head_dim, float* out, float* lse, void* stream) {
   if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
+    return SA_ERR_INVALID_ARGUMENT;
   if (idx->hkv <= 0 || hq <= 0 || hq % idx->hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0) return SA_ERR_BLOCK_PAGE;
   if (head_dim % 4 != 0 || head_dim > 256) return SA_ERR_UNSUPPORTED;
@@ -343,6 +360,7 @@ sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m
   a.inv = idx->inv;
   a.edge_head_base = idx->edge_head_base;
   a.o_partial = o_partial;
+  a.o_bf16 = partial_dtype == SA_DTYPE_BF16 ? 1 : 0;
   a.m_partial = m_partial;
   a.l_partial = l_partial;
   a.tq = idx->tq;
@@ -356,16 +374,25 @@ sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_pages,
-                             int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
-                             const int32_t* selected, const int64_t* cu_seqlens_q_host,
-                             const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
-                             const int32_t* block_tables, int32_t hq, int32_t head_dim,
-                             int32_t block_size, int32_t page_size, float softmax_scale,
-                             int32_t causal, int32_t split_edges, float* o_partial,
-                             float* m_partial, float* l_partial, float* out, float* lse,
-                             sa_path path, void* stream) {
+sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m_partial,
+                     const float* l_partial, int32_t hq, int32_t head_dim, float* out, float* lse,
+                     void* stream) {
+  return sa_combine_ex(idx, SA_DTYPE_F32, o_partial, m_partial, l_partial, hq, head_dim, out, lse,
+                       stream);
+}
+
+sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void* v_pages,
+                                int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                                const int32_t* selected, const int64_t* cu_seqlens_q_host,
+                                const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                                const int32_t* block_tables, int32_t hq, int32_t head_dim,
+                                int32_t block_size, int32_t page_size, float softmax_scale,
+                                int32_t causal, int32_t split_edges, sa_dtype partial_dtype,
+                                void* o_partial, float* m_partial, float* l_partial, float* out,
+                                float* lse, sa_path path, void* stream) {
   if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
+    return SA_ERR_INVALID_ARGUMENT;
   const int32_t hkv = idx->hkv;
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
@@ -384,12 +411,14 @@ sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
   }
   if (!fused) {
-    const sa_status st = sa_forward(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables,
-                                    cu_seqlens_q, used_kv_lens, hq, hkv, head_dim, block_size,
-                                    page_size, softmax_scale, causal, o_partial, m_partial,
-                                    l_partial, path, stream);
+    const sa_status st = sa_forward_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx,
+                                       block_tables, cu_seqlens_q, used_kv_lens, hq, hkv,
+                                       head_dim, block_size, page_size, softmax_scale, causal,
+                                       partial_dtype, o_partial, m_partial, l_partial, path,
+                                       stream);
     if (st != SA_OK) return st;
-    return sa_combine(idx, o_partial, m_partial, l_partial, hq, head_dim, out, lse, stream);
+    return sa_combine_ex(idx, partial_dtype, o_partial, m_partial, l_partial, hq, head_dim, out,
+                         lse, stream);
   }
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !selected || !o_partial ||
       !m_partial || !l_partial || !out || !idx->inv || !idx->workspace || !idx->totals)
@@ -448,6 +477,7 @@ sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_
   a.item_cnt = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(idx->workspace) +
                                            sa::workspace_layout(hkv, batch, tq, 0, 1).item_cnt);
   a.part_o = o_partial;
+  a.part_bf16 = partial_dtype == SA_DTYPE_BF16 ? 1 : 0;
   a.part_m = m_partial;
   a.part_l = l_partial;
   a.out = out;
@@ -458,19 +488,37 @@ sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
-                       int64_t num_pages, sa_dtype kv_dtype, const int32_t* selected, int64_t tq,
-                       int32_t topk, const int64_t* cu_seqlens_q_host,
-                       const int64_t* cu_seqlens_q, int32_t batch, const int32_t* used_kv_lens,
-                       const int32_t* block_tables, int32_t max_pages, int32_t hq, int32_t hkv,
-                       int32_t head_dim, int32_t block_size, int32_t page_size,
-                       float softmax_scale, int32_t causal, int32_t split_edges, sa_index* idx,
-                       float* o_partial, float* m_partial, float* l_partial, float* out,
-                       float* lse, sa_path path, void* stream) {
+sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_pages,
+                             int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                             const int32_t* selected, const int64_t* cu_seqlens_q_host,
+                             const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                             const int32_t* block_tables, int32_t hq, int32_t head_dim,
+                             int32_t block_size, int32_t page_size, float softmax_scale,
+                             int32_t causal, int32_t split_edges, float* o_partial,
+                             float* m_partial, float* l_partial, float* out, float* lse,
+                             sa_path path, void* stream) {
+  return sa_forward_combine_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                               cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                               head_dim, block_size, page_size, softmax_scale, causal,
+                               split_edges, SA_DTYPE_F32, o_partial, m_partial, l_partial, out,
+                               lse, path, stream);
+}
+
+sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pages,
+                          int64_t num_pages, sa_dtype kv_dtype, const int32_t* selected, int64_t tq,
+                          int32_t topk, const int64_t* cu_seqlens_q_host,
+                          const int64_t* cu_seqlens_q, int32_t batch, const int32_t* used_kv_lens,
+                          const int32_t* block_tables, int32_t max_pages, int32_t hq, int32_t hkv,
+                          int32_t head_dim, int32_t block_size, int32_t page_size,
+                          float softmax_scale, int32_t causal, int32_t split_edges, sa_index* idx,
+                          sa_dtype partial_dtype, void* o_partial, float* m_partial,
+                          float* l_partial, float* out, float* lse, sa_path path, void* stream) {
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return SA_ERR_BLOCK_PAGE;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
+  if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
+    return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   // Shape checks of the forward step, before any device work.
   bool fused = false;
@@ -488,10 +536,27 @@ sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
                                       batch, used_kv_lens, max_pages, block_size, page_size,
                                       split_edges, idx, stream);
   if (st != SA_OK) return st;
-  return sa_forward_combine(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
-                            cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
-                            head_dim, block_size, page_size, softmax_scale, causal, split_edges,
-                            o_partial, m_partial, l_partial, out, lse, path, stream);
+  return sa_forward_combine_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                               cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                               head_dim, block_size, page_size, softmax_scale, causal,
+                               split_edges, partial_dtype, o_partial, m_partial, l_partial, out,
+                               lse, path, stream);
+}
+
+sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
+                       int64_t num_pages, sa_dtype kv_dtype, const int32_t* selected, int64_t tq,
+                       int32_t topk, const int64_t* cu_seqlens_q_host,
+                       const int64_t* cu_seqlens_q, int32_t batch, const int32_t* used_kv_lens,
+                       const int32_t* block_tables, int32_t max_pages, int32_t hq, int32_t hkv,
+                       int32_t head_dim, int32_t block_size, int32_t page_size,
+                       float softmax_scale, int32_t causal, int32_t split_edges, sa_index* idx,
+                       float* o_partial, float* m_partial, float* l_partial, float* out,
+                       float* lse, sa_path path, void* stream) {
+  return sa_attention_ex(q, k_pages, v_pages, num_pages, kv_dtype, selected, tq, topk,
+                         cu_seqlens_q_host, cu_seqlens_q, batch, used_kv_lens, block_tables,
+                         max_pages, hq, hkv, head_dim, block_size, page_size, softmax_scale,
+                         causal, split_edges, idx, SA_DTYPE_F32, o_partial, m_partial, l_partial,
+                         out, lse, path, stream);
 }
 
 sa_status sa_get_status(const sa_index* idx, void* stream) {

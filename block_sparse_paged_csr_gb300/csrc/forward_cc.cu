@@ -260,7 +260,7 @@ forward_cc_kernel(ForwardArgs a) {
           acc.z = fmaf(p, vv.z, acc.z);
           acc.w = fmaf(p, vv.w, acc.w);
         }
-        reinterpret_cast<float4*>(a.o_partial + (row0 + rg + r) * d)[c] = acc;
+        store_o4(a.o_partial, a.o_bf16, (row0 + rg + r) * d + 4 * c, acc);
       }
       __syncthreads();
     }

@@ -322,7 +322,7 @@ forward_dec_kernel(ForwardArgs a) {
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
           if (r < rows_g) {
-            reinterpret_cast<float4*>(a.o_partial + (row0 + r) * kD)[lane] = o[r];
+            store_o4(a.o_partial, a.o_bf16, (row0 + r) * kD + 4 * lane, o[r]);
             if (lane == 0) {
               a.m_partial[row0 + r] = m_run[r] == -INFINITY ? -INFINITY : m_run[r] * kLn2;
               a.l_partial[row0 + r] = l;

@@ -94,7 +94,8 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = bf2(x0 - bf_lo_f(hi), x1 - bf_hi_f(hi));
 }
 
-template <int R, int NST, int WARPS>
+// kOBf16: the o partials are written as bf16.
+template <int R, int NST, int WARPS, bool kOBf16>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 forward_dec_mma_kernel(ForwardArgs a) {
   static_assert(R == 8 || R == 16, "rows per group");
@@ -375,10 +376,17 @@ forward_dec_mma_kernel(ForwardArgs a) {
           l += __shfl_xor_sync(0xffffffffu, l, 2);
           const int r = g + 8 * h2;
           if (r < rows_g) {
-            float* dst = a.o_partial + (row0 + r) * kD + 2 * c;
+            if constexpr (kOBf16) {
+              uint16_t* dst = static_cast<uint16_t*>(a.o_partial) + (row0 + r) * kD + 2 * c;
 #pragma unroll
-            for (int nt = 0; nt < 16; ++nt)
-              *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(o[nt][2 * h2], o[nt][2 * h2 + 1]);
+              for (int nt = 0; nt < 16; ++nt)
+                *reinterpret_cast<uint32_t*>(dst + 8 * nt) = bf2(o[nt][2 * h2], o[nt][2 * h2 + 1]);
+            } else {
+              float* dst = static_cast<float*>(a.o_partial) + (row0 + r) * kD + 2 * c;
+#pragma unroll
+              for (int nt = 0; nt < 16; ++nt)
+                *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(o[nt][2 * h2], o[nt][2 * h2 + 1]);
+            }
             if (c == 0) {
               a.m_partial[row0 + r] = m_run[h2] == -INFINITY ? -INFINITY : m_run[h2] * kLn2;
               a.l_partial[row0 + r] = l;
@@ -396,12 +404,12 @@ forward_dec_mma_kernel(ForwardArgs a) {
   }
 }
 
-template <int R, int NST, int WARPS>
+template <int R, int NST, int WARPS, bool kOBf16>
 cudaError_t launch_dec_mma(const ForwardArgs& a, cudaStream_t stream) {
   const MmaPlan p = mma_plan(R, NST);
   const size_t smem = p.warp_bytes * WARPS;
   if (smem > 227 * 1024) return cudaErrorNotSupported;
-  const void* fn = reinterpret_cast<const void*>(forward_dec_mma_kernel<R, NST, WARPS>);
+  const void* fn = reinterpret_cast<const void*>(forward_dec_mma_kernel<R, NST, WARPS, kOBf16>);
   cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -412,7 +420,7 @@ cudaError_t launch_dec_mma(const ForwardArgs& a, cudaStream_t stream) {
   const int64_t need = (a.max_splits + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  forward_dec_mma_kernel<R, NST, WARPS>
+  forward_dec_mma_kernel<R, NST, WARPS, kOBf16>
       <<<static_cast<unsigned>(grid), WARPS * 32, smem, stream>>>(a);
   return cudaGetLastError();
 }
@@ -431,8 +439,11 @@ bool forward_dec_mma_supported(int head_dim, int block_size, int page_size, int 
 cudaError_t launch_forward_dec_mma(const ForwardArgs& a, cudaStream_t stream) {
   if (!forward_dec_mma_supported(a.head_dim, a.block_size, a.page_size, a.qhead, a.kv_bf16))
     return cudaErrorNotSupported;
-  if (a.qhead <= 8) return launch_dec_mma<8, 3, 6>(a, stream);
-  return launch_dec_mma<16, 3, 4>(a, stream);
+  if (a.qhead <= 8)
+    return a.o_bf16 ? launch_dec_mma<8, 3, 6, true>(a, stream)
+                    : launch_dec_mma<8, 3, 6, false>(a, stream);
+  return a.o_bf16 ? launch_dec_mma<16, 3, 4, true>(a, stream)
+                  : launch_dec_mma<16, 3, 4, false>(a, stream);
 }
 
 }  // namespace sa

@@ -163,13 +163,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int rows, int r, int k) {
   return static_cast<uint32_t>(panel * rows * 128 + r * 128 + ((chunk ^ (r & 7)) << 4) + within);
 }
 
-// Two f32 values to a packed bf16x2 (round to nearest even), `lo` in the low half.
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Four K/V elements (f32 or bf16) as packed bf16 (round to nearest even).
 template <bool kBf16>
 __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off) {
@@ -550,11 +543,12 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
     if (!__all_sync(0xffffffffu, got)) return false;
     tc_fence_after();
     const uint32_t t_o = tmem + 256 + 128 * sb + lane_base;
-    // 16 columns at a time: each thread puts 16 of its row's values into the
-    // warp's staging tile (16-byte chunk i of row r at i ^ ((r >> 1) & 3), so
-    // 8 consecutive rows hit 8 different bank groups), then the warp writes
-    // 8 rows x 64 bytes per store instruction.  Valid rows are a prefix of
-    // the tile, so a warp with a valid row has lane 0 valid.
+    // 64 bytes of a row at a time (16 f32 or 32 bf16 columns): each thread
+    // puts them into the warp's staging tile (16-byte chunk i of row r at
+    // i ^ ((r >> 1) & 3), so 8 consecutive rows hit 8 different bank
+    // groups), then the warp writes 8 rows x 64 bytes per store instruction.
+    // Valid rows are a prefix of the tile, so a warp with a valid row has
+    // lane 0 valid.
     const int64_t prow0 = __shfl_sync(0xffffffffu, prow, 0);
     const unsigned live = __ballot_sync(0xffffffffu, prow >= 0);
 #pragma unroll 1
@@ -562,6 +556,28 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
       float v[32];
       tmem_ld32(t_o + c * 32, v);
       tmem_ld_wait();
+      if (a.o_bf16) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4*>(wst + lane * 16)[i ^ ((lane >> 1) & 3)] =
+              make_uint4(pack_bf16x2_rn(v[8 * i], v[8 * i + 1]),
+                         pack_bf16x2_rn(v[8 * i + 2], v[8 * i + 3]),
+                         pack_bf16x2_rn(v[8 * i + 4], v[8 * i + 5]),
+                         pack_bf16x2_rn(v[8 * i + 6], v[8 * i + 7]));
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = 8 * k + (lane >> 2);
+          const int ch = lane & 3;
+          if ((live >> r) & 1u) {
+            const uint4 val = reinterpret_cast<const uint4*>(wst + r * 16)[ch ^ ((r >> 1) & 3)];
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o_partial) + (prow0 + r) * kD +
+                                     c * 32)[ch] = val;
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         __syncwarp();
@@ -577,7 +593,8 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
           const int ch = lane & 3;
           if ((live >> r) & 1u) {
             const float4 val = reinterpret_cast<const float4*>(wst + r * 16)[ch ^ ((r >> 1) & 3)];
-            reinterpret_cast<float4*>(a.o_partial + (prow0 + r) * kD + c * 32 + 16 * hf)[ch] = val;
+            reinterpret_cast<float4*>(static_cast<float*>(a.o_partial) + (prow0 + r) * kD +
+                                      c * 32 + 16 * hf)[ch] = val;
           }
         }
       }

@@ -430,7 +430,7 @@ __device__ void merge_warp(const FusedDecArgs& a, const Smem& sm, int lane) {
         write_row(a, row0 + r, lane, M, l, o);
       } else {
         const int64_t pr = prow + static_cast<int64_t>(k) * qhead + r;
-        reinterpret_cast<float4*>(a.part_o + pr * kD)[lane] = o;
+        store_o4(a.part_o, a.part_bf16, pr * kD + 4 * lane, o);
         if (lane == 0) {
           a.part_m[pr] = M;
           a.part_l[pr] = l;
@@ -476,10 +476,14 @@ __device__ void merge_warp(const FusedDecArgs& a, const Smem& sm, int lane) {
             for (int t = 0; t < 8; ++t) {
               wt[t] = __shfl_sync(0xffffffffu, e, (t0 + t) & 31);
               v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (t0 + t < n && wt[t] > 0.f)
-                v[t] = __ldcg(reinterpret_cast<const float4*>(
-                                  a.part_o + (pr0 + static_cast<int64_t>(b + t0 + t) * qhead) * kD) +
-                              lane);
+              if (t0 + t < n && wt[t] > 0.f) {
+                const int64_t e = (pr0 + static_cast<int64_t>(b + t0 + t) * qhead) * kD + 4 * lane;
+                v[t] = a.part_bf16
+                           ? bf16x4_to_f32(__ldcg(reinterpret_cast<const uint2*>(
+                                 static_cast<const uint16_t*>(a.part_o) + e)))
+                           : __ldcg(reinterpret_cast<const float4*>(
+                                 static_cast<const float*>(a.part_o) + e));
+              }
             }
 #pragma unroll
             for (int t = 0; t < 8; ++t) {

@@ -69,7 +69,8 @@ struct ForwardArgs {
   int64_t* totals;          // [0] E, [1] splits, [3] status
   int64_t max_splits;       // capacity of the split list (upper bound of totals[1])
   // outputs
-  float* o_partial;
+  void* o_partial;          // f32, or bf16 when o_bf16
+  int o_bf16;
   float* m_partial;
   float* l_partial;
 };
@@ -113,7 +114,8 @@ struct FusedDecArgs {
   float scale;
   int64_t* status;          // device status word
   uint32_t* item_cnt;       // [tq * hkv], zero on entry, left zero
-  float* part_o;            // per-piece scratch rows (the partial buffers)
+  void* part_o;             // per-piece scratch rows (the partial buffers):
+  int part_bf16;            // o rows f32, or bf16 when part_bf16
   float* part_m;
   float* part_l;
   float* out;
@@ -130,7 +132,8 @@ cudaError_t launch_fused_dec(const FusedDecArgs& a, cudaStream_t stream);
 struct CombineArgs {
   const int32_t* inv;
   const int64_t* edge_head_base;
-  const float* o_partial;
+  const void* o_partial;    // f32, or bf16 when o_bf16
+  int o_bf16;
   const float* m_partial;
   const float* l_partial;
   int64_t tq;

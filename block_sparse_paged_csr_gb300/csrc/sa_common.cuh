@@ -116,4 +116,22 @@ __device__ __forceinline__ float4 bf16x4_to_f32(uint2 u) {
   return r;
 }
 
+// Two f32 values to a packed bf16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four consecutive elements of a partial o buffer, starting at element `off`
+// (a multiple of 4): f32, or bf16 rounded to nearest even when the caller
+// asked for 16-bit o partials.
+__device__ __forceinline__ void store_o4(void* o, int bf16, int64_t off, float4 v) {
+  if (bf16)
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(o) + off) =
+        make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+  else
+    *reinterpret_cast<float4*>(static_cast<float*>(o) + off) = v;
+}
+
 }  // namespace sa

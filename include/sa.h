@@ -253,6 +253,26 @@ sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
                      void *stream);
 
 /*
+ * sa_forward with the o partials stored as `partial_dtype`: SA_DTYPE_F32
+ * (exactly sa_forward) or SA_DTYPE_BF16, where each o value is rounded to
+ * nearest even bfloat16 as it is written and o_partial holds
+ * [tq*hkv*topk*qhead, head_dim] uint16 bit patterns (16-byte aligned).  m and
+ * l stay float32.  The pages keep all partials in f32 (forward.rs, the
+ * o_partial / m_partial / l_partial buffers); the 16-bit form has no
+ * counterpart there: it is an opt-in that halves the bytes the forward
+ * writes and the combine reads, at a relative error of at most 2^-8 per o
+ * value before the combine.  Every forward kernel supports it.  Other
+ * partial_dtype values: SA_ERR_INVALID_ARGUMENT.
+ */
+sa_status sa_forward_ex(const float *q, const void *k_pages, const void *v_pages,
+                        int64_t num_pages, sa_dtype kv_dtype, const sa_index *idx,
+                        const int32_t *block_tables, const int64_t *cu_seqlens_q,
+                        const int32_t *used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
+                        int32_t block_size, int32_t page_size, float softmax_scale,
+                        int32_t causal, sa_dtype partial_dtype, void *o_partial,
+                        float *m_partial, float *l_partial, sa_path path, void *stream);
+
+/*
  * Name of the kernel sa_forward launches for a problem of tq queries in
  * `batch` sequences with these head counts, sizes, K/V type and `path`
  * ("forward_dec_mma_kernel", "forward_tc_kernel", "forward_dec_kernel" or
@@ -296,6 +316,18 @@ sa_status sa_forward_combine(const float *q, const void *k_pages, const void *v_
                              float *m_partial, float *l_partial, float *out, float *lse,
                              sa_path path, void *stream);
 
+/* sa_forward_combine with o partials of `partial_dtype` (see sa_forward_ex);
+ * on the fused decode path the pieces' scratch o rows take that type. */
+sa_status sa_forward_combine_ex(const float *q, const void *k_pages, const void *v_pages,
+                                int64_t num_pages, sa_dtype kv_dtype, const sa_index *idx,
+                                const int32_t *selected, const int64_t *cu_seqlens_q_host,
+                                const int64_t *cu_seqlens_q, const int32_t *used_kv_lens,
+                                const int32_t *block_tables, int32_t hq, int32_t head_dim,
+                                int32_t block_size, int32_t page_size, float softmax_scale,
+                                int32_t causal, int32_t split_edges, sa_dtype partial_dtype,
+                                void *o_partial, float *m_partial, float *l_partial, float *out,
+                                float *lse, sa_path path, void *stream);
+
 /*
  * Step 3: log-sum-exp combine (forward.rs module doc: "standard FlashAttention
  * log-sum-exp update").  For query i and q-head hq (h = hq / qhead), over
@@ -309,6 +341,13 @@ sa_status sa_forward_combine(const float *q, const void *k_pages, const void *v_
 sa_status sa_combine(const sa_index *idx, const float *o_partial, const float *m_partial,
                      const float *l_partial, int32_t hq, int32_t head_dim, float *out,
                      float *lse, void *stream);
+
+/* sa_combine over o partials of `partial_dtype` (SA_DTYPE_F32: exactly
+ * sa_combine; SA_DTYPE_BF16: the uint16 rows sa_forward_ex writes), widened
+ * to f32 as they are read; other values: SA_ERR_INVALID_ARGUMENT. */
+sa_status sa_combine_ex(const sa_index *idx, sa_dtype partial_dtype, const void *o_partial,
+                        const float *m_partial, const float *l_partial, int32_t hq,
+                        int32_t head_dim, float *out, float *lse, void *stream);
 
 /*
  * Steps 1-3 on one stream, no host synchronisation (kvouter_attention, the
@@ -340,6 +379,19 @@ sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,
                        float softmax_scale, int32_t causal, int32_t split_edges, sa_index *idx,
                        float *o_partial, float *m_partial, float *l_partial, float *out,
                        float *lse, sa_path path, void *stream);
+
+/* sa_attention with o partials of `partial_dtype` (see sa_forward_ex); the
+ * o_partial buffer is [tq*hkv*topk*qhead, head_dim] of that type. */
+sa_status sa_attention_ex(const float *q, const void *k_pages, const void *v_pages,
+                          int64_t num_pages, sa_dtype kv_dtype, const int32_t *selected,
+                          int64_t tq, int32_t topk, const int64_t *cu_seqlens_q_host,
+                          const int64_t *cu_seqlens_q, int32_t batch,
+                          const int32_t *used_kv_lens, const int32_t *block_tables,
+                          int32_t max_pages, int32_t hq, int32_t hkv, int32_t head_dim,
+                          int32_t block_size, int32_t page_size, float softmax_scale,
+                          int32_t causal, int32_t split_edges, sa_index *idx,
+                          sa_dtype partial_dtype, void *o_partial, float *m_partial,
+                          float *l_partial, float *out, float *lse, sa_path path, void *stream);
 
 /* Synchronises `stream` and returns the first device-detected error recorded
  * in idx->totals[3] (SA_OK if none), or SA_ERR_CUDA if the stream failed. */

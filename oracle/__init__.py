@@ -89,6 +89,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                  p, i64, p, i64, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, p, p, p])
     lib.orc_forward.restype = ctypes.c_int
+    lib.orc_round_bf16.argtypes = [ctypes.c_double]
+    lib.orc_round_bf16.restype = ctypes.c_double
+    lib.orc_round_bf16_array.argtypes = [p, i64, p]
+    lib.orc_round_bf16_array.restype = None
     lib.orc_combine.argtypes = [p, p, i64, i64, i64, i64, i64, p, p, p, p, p]
     lib.orc_combine.restype = None
     lib.orc_direct.argtypes = ([p, p, p, ctypes.c_int, i64, p, i64, i64, i64, p, i64, p, p,
@@ -228,9 +232,23 @@ def _kv(pages):
     return np.ascontiguousarray(a, dtype=np.float32), 0
 
 
+def round_bf16(x, _lib=None):
+    """Each value rounded to the nearest bfloat16 (ties to even), as float64."""
+    L = _lib or lib()
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(a)
+    if a.size:
+        L.orc_round_bf16_array(_ptr(a), a.size, _ptr(y))
+    return y
+
+
 def forward(q, k_pages, v_pages, index: dict, block_tables, cu_seqlens_q, used_kv_lens,
-            hq: int, head_dim: int, softmax_scale: float, causal: bool, _lib=None):
-    """Partials (o [E*qhead, d], m [E*qhead], l [E*qhead]) in float64."""
+            hq: int, head_dim: int, softmax_scale: float, causal: bool, partial_dtype="f32",
+            _lib=None):
+    """Partials (o [E*qhead, d], m [E*qhead], l [E*qhead]) in float64;
+    ``partial_dtype="bf16"``: o rounded to bfloat16 (the opt-in 16-bit o
+    partials; m and l unchanged)."""
+    assert partial_dtype in ("f32", "bf16")
     L = _lib or lib()
     qa = _c(q, np.float32)
     k, kb = _kv(k_pages)
@@ -259,7 +277,10 @@ def forward(q, k_pages, v_pages, index: dict, block_tables, cu_seqlens_q, used_k
                          cu.size - 1, _ptr(used), hq, hkv, head_dim, block_size, page_size,
                          softmax_scale, int(bool(causal)), _ptr(o), _ptr(m), _ptr(l))
     _check(code)
-    return o[: E * qhead], m[: E * qhead], l[: E * qhead]
+    o = o[: E * qhead]
+    if partial_dtype == "bf16":
+        o = round_bf16(o, _lib=L)
+    return o, m[: E * qhead], l[: E * qhead]
 
 
 # --------------------------------------------------------------------------- step 3
@@ -284,14 +305,14 @@ def combine(index: dict, qhead: int, head_dim: int, o, m, l, _lib=None):
 
 def attention(q, k_pages, v_pages, selected, block_tables, cu_seqlens_q, used_kv_lens,
               hq, head_dim, block_size, page_size, softmax_scale, causal, split_edges=0,
-              _lib=None):
+              partial_dtype="f32", _lib=None):
     """Steps 1-3 in sequence: (out, lse, index, (o, m, l))."""
     bt = np.asarray(block_tables)
     idx = build_index(selected, cu_seqlens_q, used_kv_lens, bt.shape[1], block_size,
                       page_size, split_edges, _lib=_lib)
     qhead = hq // idx["hkv"]
     o, m, l = forward(q, k_pages, v_pages, idx, bt, cu_seqlens_q, used_kv_lens, hq,
-                      head_dim, softmax_scale, causal, _lib=_lib)
+                      head_dim, softmax_scale, causal, partial_dtype=partial_dtype, _lib=_lib)
     out, lse = combine(idx, qhead, head_dim, o, m, l, _lib=_lib)
     return out, lse, idx, (o, m, l)
 

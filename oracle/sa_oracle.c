@@ -32,6 +32,9 @@
  *   - Work splits: each non-empty slot, in CSR order, cut into consecutive
  *     pieces of at most `split_edges` edges (0 = never cut).
  *   - Combine of a row with no live partial gives out = 0 and lse = -inf.
+ *   - 16-bit o partials (an opt-in the pages do not have; they keep o, m, l
+ *     in f32): each o value is the nearest bfloat16 to the exact one, ties
+ *     to even; m and l are kept exactly.
  *
  * Parity pins: see tests/test_oracle_pins.py (dense attention on tiny inputs,
  * permutation / padding invariance, single block, equal-key closed form,
@@ -115,6 +118,35 @@ static double kv_value(const void *pages, int kv_is_bf16, int64_t offset)
     if (kv_is_bf16)
         return bf16_bits_to_double(((const uint16_t *)pages)[offset]);
     return (double)((const float *)pages)[offset];
+}
+
+/*
+ * Nearest bfloat16 value of x, ties to even: bfloat16 keeps the sign and
+ * 8-bit exponent range of binary32 with 8 significant bits, so a normal value
+ * in [2^e, 2^(e+1)) lies on a grid of step 2^(e-7), and values below the
+ * smallest normal 2^-126 on the subnormal grid of step 2^-133.  Results at
+ * or beyond 2^128 overflow to infinity.  Used for the opt-in 16-bit o
+ * partials.
+ */
+double orc_round_bf16(double x)
+{
+    if (x != x || x == 0.0 || isinf(x))
+        return x;
+    int k;
+    frexp(x, &k);                 /* |x| = f 2^k, f in [0.5, 1): e = k - 1 */
+    int step = k - 8;             /* log2 of the grid step 2^(e-7)         */
+    if (step < -133)
+        step = -133;
+    double y = ldexp(rint(ldexp(x, -step)), step);   /* rint: ties to even */
+    if (fabs(y) >= ldexp(1.0, 128))
+        return x > 0 ? INFINITY : -INFINITY;
+    return y;
+}
+
+void orc_round_bf16_array(const double *x, int64_t n, double *y)
+{
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = orc_round_bf16(x[i]);
 }
 
 /* ------------------------------------------------------------------------- */

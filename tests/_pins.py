@@ -462,5 +462,75 @@ def pin_errors(L):
     assert idx0["edges"].shape[0] == 0 and np.all(out == 0) and np.all(np.isneginf(lse))
 
 
+def pin_round_bf16(L):
+    """Nearest-bfloat16 rounding against the library conversion float32 ->
+    bfloat16 (round to nearest even) on normal, subnormal, huge and tie
+    values, plus hand-checked ties and limits."""
+    import torch
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(20000).astype(np.float32)
+    ties = np.float32([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -133 * 1.5,
+                       2 ** -133 * 0.5, 2 ** -126 * (1 + 2 ** -8), 3.3895313892515355e38])
+    with np.errstate(over="ignore"):
+        x = np.concatenate([x, x * np.float32(1e-39), x * np.float32(1e36), ties])
+    got = oracle.round_bf16(x.astype(np.float64), _lib=L)
+    lib = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, lib), "bf16 rounding differs from the library conversion"
+    # ties go to the even neighbour; the subnormal grid is 2^-133; the largest
+    # bf16 value stays, the next grid point overflows
+    r = lambda v: float(oracle.round_bf16(np.float64([v]), _lib=L)[0])
+    assert r(1 + 2 ** -8) == 1.0 and r(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert r(2 ** -133 * 1.5) == 2 ** -132 and r(2 ** -133 * 0.5) == 0.0
+    assert r((2 - 2 ** -7) * 2.0 ** 127) == (2 - 2 ** -7) * 2.0 ** 127
+    assert r((2 - 2 ** -8) * 2.0 ** 127) == np.inf
+    assert r(1.0 / 3.0) == 0.333984375
+
+
+def pin_bf16_partials(L, seeds=range(8)):
+    """16-bit o partials: each combined output moves from the f32-partial one
+    by at most 2^-8 sum_r w_r |o_r| / L (every o value carries a relative
+    rounding error of at most 2^-8), and does move; with bf16 V and blocks of
+    one live key, o = v is a bfloat16 value already and nothing changes."""
+    for s in seeds:
+        c = random_case(s, full=False, allow_empty_seq=False)
+        args = (c["q"], c["k"], c["v"], c["sel"], c["bt"], c["cu"], c["used"], c["hq"], c["d"],
+                c["bs"], c["ps"], c["scale"], bool(s % 2))
+        out, lse, idx, (o, m, l) = oracle.attention(*args, _lib=L)
+        out16, lse16, _, (o16, m16, l16) = oracle.attention(*args, partial_dtype="bf16", _lib=L)
+        assert np.array_equal(m, m16) and np.array_equal(l, l16) and np.array_equal(lse, lse16)
+        qhead = c["hq"] // c["hkv"]
+        bound = np.zeros_like(out)
+        for h in range(c["hkv"]):
+            for i in range(idx["tq"]):
+                for qh in range(qhead):
+                    rows = [(idx["edge_head_base"][h] + p) * qhead + qh
+                            for p in idx["inv"][h, i] if p >= 0]
+                    rows = [r for r in rows if np.isfinite(m[r])]
+                    if not rows:
+                        continue
+                    mm = max(m[r] for r in rows)
+                    w = [np.exp(m[r] - mm) for r in rows]
+                    big_l = sum(wi * l[r] for wi, r in zip(w, rows))
+                    bound[i, h * qhead + qh] = sum(wi * np.abs(o[r]) for wi, r in
+                                                   zip(w, rows)) / big_l
+        diff = np.abs(out16 - out)
+        assert np.all(diff <= 2.0 ** -8 * bound * (1 + 1e-9) + 1e-300), "bf16 partial bound"
+        assert np.any(diff > 0), "o partials were not rounded"
+    # bf16 V, one live key per block: o = v exactly, so nothing changes
+    c = random_case(3, bf16=True, full=False, allow_empty_seq=False)
+    c["bs"], c["ps"] = 1, 1
+    c["bt"] = np.arange(c["bt"].shape[0] * c["bt"].shape[1], dtype=np.int32).reshape(
+        c["bt"].shape) % (c["k"].shape[0])
+    msb = c["bt"].shape[1]
+    c["used"] = np.full(len(c["cu"]) - 1, msb, np.int32)
+    c["sel"] = np.random.default_rng(3).integers(-1, msb, size=c["sel"].shape).astype(np.int32)
+    args = (c["q"], c["k"], c["v"], c["sel"], c["bt"], c["cu"], c["used"], c["hq"], c["d"],
+            c["bs"], c["ps"], c["scale"], False)
+    out, _, _, (o, _, _) = oracle.attention(*args, _lib=L)
+    out16, _, _, (o16, _, _) = oracle.attention(*args, partial_dtype="bf16", _lib=L)
+    assert np.array_equal(o, o16) and np.array_equal(out, out16)
+
+
 ALL_PINS = [pin_types, pin_dense_fixtures, pin_dense_random, pin_invariance, pin_single_block,
-            pin_equal_keys, pin_partials, pin_index_bruteforce, pin_errors]
+            pin_equal_keys, pin_partials, pin_index_bruteforce, pin_errors, pin_round_bf16,
+            pin_bf16_partials]

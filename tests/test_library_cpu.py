@@ -122,6 +122,51 @@ def test_forward_and_combine_host_checks(lib):
         names["UNSUPPORTED"]
 
 
+def test_partial_dtype_host_checks(lib):
+    """The 16-bit-partial entries: the same checks as their f32 forms, plus
+    partial_dtype itself (f32 or bf16 only), all before any launch."""
+    from block_sparse_paged_csr_gb300 import _native
+
+    names = {v: k for k, v in _native.STATUS_NAMES.items()}
+    idx = _native.SaIndex(hkv=2, pages_per_block=2, block_size=32, page_size=16, tq=4, topk=2)
+
+    def fwd(pdt, hq=4, d=32):
+        return lib.sa_forward_ex(None, None, None, 16, 0, ctypes.byref(idx), None, None, None, hq,
+                                 2, d, 32, 16, 0.1, 0, pdt, None, None, None, 0, None)
+
+    assert fwd(2) == names["INVALID_ARGUMENT"]
+    assert fwd(-1) == names["INVALID_ARGUMENT"]
+    assert fwd(1, hq=3) == names["HEAD_COUNT"]
+    assert fwd(1, d=30) == names["UNSUPPORTED"]
+    assert fwd(1) == names["INVALID_ARGUMENT"]       # null pointers
+    comb = lib.sa_combine_ex
+    assert comb(ctypes.byref(idx), 2, None, None, None, 4, 32, None, None, None) == \
+        names["INVALID_ARGUMENT"]
+    assert comb(ctypes.byref(idx), 1, None, None, None, 3, 32, None, None, None) == \
+        names["HEAD_COUNT"]
+    assert comb(ctypes.byref(idx), 1, None, None, None, 4, 32, None, None, None) == \
+        names["INVALID_ARGUMENT"]
+    host_cu = np.array([0, 4], np.int64)
+    assert lib.sa_attention_ex(None, None, None, 16, 0, None, 4, 2, host_cu.ctypes.data, None, 1,
+                               None, None, 4, 4, 2, 32, 32, 16, 0.1, 0, 0, ctypes.byref(idx), 5,
+                               None, None, None, None, None, 0, None) == names["INVALID_ARGUMENT"]
+    assert lib.sa_forward_combine_ex(None, None, None, 16, 0, ctypes.byref(idx), None,
+                                     host_cu.ctypes.data, None, None, None, 4, 32, 32, 16, 0.1, 0,
+                                     0, 9, None, None, None, None, None, 0, None) == \
+        names["INVALID_ARGUMENT"]
+    import block_sparse_paged_csr_gb300 as sa
+    import torch
+    with pytest.raises(ValueError):
+        sa._partial_dtype("f16", None)
+    with pytest.raises(ValueError):
+        sa._partial_dtype("bf16", torch.empty(1, dtype=torch.float32))
+    with pytest.raises(TypeError):
+        sa._partial_dtype(None, torch.empty(1, dtype=torch.float16))
+    assert sa._partial_dtype(None, None) == (torch.float32, 0)
+    assert sa._partial_dtype("bf16", None) == (torch.bfloat16, 1)
+    assert sa._partial_dtype(None, torch.empty(1, dtype=torch.bfloat16)) == (torch.bfloat16, 1)
+
+
 def test_forward_kernel_choice(lib):
     """The kernel each serving workload takes under SA_PATH_AUTO and under
     each forced path, and refusals where sa_forward would refuse."""

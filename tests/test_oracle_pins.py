@@ -60,6 +60,11 @@ MUTATIONS = [
      "for (int64_t slot = nbs - 1; slot >= 0; --slot)"),
     ("lse uses natural log of max only", "lse[i * hq + hq_abs] = big_m + log(big_l);",
      "lse[i * hq + hq_abs] = big_m;"),
+    ("bf16 rounding truncates", "double y = ldexp(rint(ldexp(x, -step)), step);",
+     "double y = ldexp(trunc(ldexp(x, -step)), step);"),
+    ("bf16 grid one bit too fine", "int step = k - 8;", "int step = k - 9;"),
+    ("bf16 subnormal grid too coarse", "if (step < -133)\n        step = -133;",
+     "if (step < -126)\n        step = -126;"),
 ]
 
 
