@@ -218,7 +218,7 @@ __host__ __device__ inline TcPlan tc_plan(int bs) {
   p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * 2, 128);     // int32 [kvb][BS]
   p.info = tc_up(p.kpos + kvb * static_cast<size_t>(bs) * 4, 128);      // UnitInfo [kvb]
   p.koff = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // int64 [BS]
-  p.stage = tc_up(p.koff + static_cast<size_t>(bs) * 8, 128);           // f32 [8][32][16]
+  p.stage = tc_up(p.koff + static_cast<size_t>(bs) * 8, 1024);          // f32 [8][32][16]
   p.bars = tc_up(p.stage + 8 * 32 * 16 * 4, 128);                       // uint64 [32]
   p.misc = tc_up(p.bars + 32 * 8, 128);                                 // TMEM slot, unit bases
   p.total = p.misc + 16 + 201 * 4 + 1024;                               // + alignment slack
@@ -522,8 +522,9 @@ __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& 
 // Softmax warpgroup g (0 or 1) takes the tiles whose running index has
 // parity g, and with them TMEM buffers S[g], O[g].
 template <int BS>
-__device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
-                           const TcBars& B, uint32_t tmem, int64_t n_units, int warp, int lane) {
+__device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsigned char* smem,
+                           const TcPlan& P, const TcBars& B, uint32_t tmem, int64_t n_units,
+                           int warp, int lane) {
   const uint32_t g = static_cast<uint32_t>((warp - 1 - kLoaders) >> 2);
   constexpr int KVB = TcCfg<BS>::KVB;
   int64_t* status = a.totals + 3;
@@ -545,19 +546,37 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
     const uint32_t t_o = tmem + 256 + 128 * sb + lane_base;
     // 64 bytes of a row at a time (16 f32 or 32 bf16 columns): each thread
     // puts them into the warp's staging tile (16-byte chunk i of row r at
-    // i ^ ((r >> 1) & 3), so 8 consecutive rows hit 8 different bank
-    // groups), then the warp writes 8 rows x 64 bytes per store instruction.
-    // Valid rows are a prefix of the tile, so a warp with a valid row has
-    // lane 0 valid.
+    // i ^ ((r >> 1) & 3): the 64-byte swizzle of the tensor maps, and 8
+    // consecutive rows hit 8 different bank groups).  A warp whose 32 rows
+    // are all live hands the tile to the TMA engine (one 32 x 64-byte box
+    // store, asynchronous: the warp goes on while the rows drain to L2);
+    // otherwise it writes its live rows, 8 rows x 64 bytes per store
+    // instruction.  Valid rows are a prefix of the tile, so a warp with a
+    // valid row has lane 0 valid.
     const int64_t prow0 = __shfl_sync(0xffffffffu, prow, 0);
     const unsigned live = __ballot_sync(0xffffffffu, prow >= 0);
+    const bool by_tma = a.o_tma && live == 0xffffffffu;
+    // the staging tile is free once this thread's earlier box stores have
+    // read it (lane 0 issues them)
+    auto stage_free = [&]() {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    };
+    auto stage_store = [&](int x) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(omap, x, static_cast<int>(prow0), wst);
+        bulk_commit();
+      }
+    };
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       float v[32];
       tmem_ld32(t_o + c * 32, v);
       tmem_ld_wait();
       if (a.o_bf16) {
-        __syncwarp();
+        stage_free();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           reinterpret_cast<uint4*>(wst + lane * 16)[i ^ ((lane >> 1) & 3)] =
@@ -565,6 +584,10 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
                          pack_bf16x2_rn(v[8 * i + 2], v[8 * i + 3]),
                          pack_bf16x2_rn(v[8 * i + 4], v[8 * i + 5]),
                          pack_bf16x2_rn(v[8 * i + 6], v[8 * i + 7]));
+        if (by_tma) {
+          stage_store(c * 32);
+          continue;
+        }
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -580,12 +603,16 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
       }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        __syncwarp();
+        stage_free();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           reinterpret_cast<float4*>(wst + lane * 16)[i ^ ((lane >> 1) & 3)] =
               make_float4(v[16 * hf + 4 * i], v[16 * hf + 4 * i + 1], v[16 * hf + 4 * i + 2],
                           v[16 * hf + 4 * i + 3]);
+        if (by_tma) {
+          stage_store(c * 32 + 16 * hf);
+          continue;
+        }
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -730,7 +757,7 @@ __device__ void tc_softmax(const ForwardArgs& a, unsigned char* smem, const TcPl
 
 template <int BS, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
-forward_tc_kernel(ForwardArgs a) {
+forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   constexpr int KVB = TcCfg<BS>::KVB;
   constexpr int kNX = TcCfg<BS>::NX;
   extern __shared__ unsigned char smem_raw[];
@@ -804,7 +831,9 @@ forward_tc_kernel(ForwardArgs a) {
   } else if (warp <= kLoaders) {
     tc_loader<BS, kBf16>(a, smem, P, B, unit_base, n_units, warp - 1, lane);
   } else {
-    tc_softmax<BS>(a, smem, P, B, tmem, n_units, warp, lane);
+    tc_softmax<BS>(a, &omap, smem, P, B, tmem, n_units, warp, lane);
+    // box stores issued by this thread have landed before the CTA leaves
+    bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -823,11 +852,32 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
   err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
+  // The partial o rows [capacity, 128] as a 2-D tensor map for the
+  // epilogue's box stores (32 rows x 64 bytes, 64-byte swizzle); without one
+  // (capacity outside int32 coordinates, or no encoder) every row goes out
+  // through plain stores.
+  ForwardArgs args = a;
+  args.o_tma = 0;
+  CUtensorMap omap{};
+  const int64_t cap = a.max_splits * a.qhead;
+  EncodeTiledFn enc = encode_fn();
+  if (enc != nullptr && cap >= 32 && cap < (int64_t{1} << 31)) {
+    const cuuint64_t dims[2] = {kD, static_cast<cuuint64_t>(cap)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * (a.o_bf16 ? 2 : 4)};
+    const cuuint32_t box[2] = {a.o_bf16 ? 32u : 16u, 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&omap, a.o_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+            2, a.o_partial, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      args.o_tma = 1;
+  }
   // One CTA per SM: it holds all 512 TMEM columns.
   int64_t grid = device_sm_count();
   if (grid > a.max_splits) grid = a.max_splits;
   if (grid < 1) grid = 1;
-  forward_tc_kernel<BS, kBf16><<<static_cast<unsigned>(grid), kThreads, p.total, stream>>>(a);
+  forward_tc_kernel<BS, kBf16>
+      <<<static_cast<unsigned>(grid), kThreads, p.total, stream>>>(omap, args);
   return cudaGetLastError();
 }
 

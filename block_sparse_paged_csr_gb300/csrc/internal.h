@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "sa.h"
@@ -71,6 +72,7 @@ struct ForwardArgs {
   // outputs
   void* o_partial;          // f32, or bf16 when o_bf16
   int o_bf16;
+  int o_tma;                // set by a launcher: o rows may go out by tensor-map stores
   float* m_partial;
   float* l_partial;
 };
@@ -145,5 +147,12 @@ struct CombineArgs {
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
 int device_sm_count();
+
+// cuTensorMapEncodeTiled from the driver (NULL if unavailable); looked up once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 
 }  // namespace sa

@@ -116,6 +116,31 @@ __device__ __forceinline__ float4 bf16x4_to_f32(uint2 u) {
   return r;
 }
 
+// Tiled tensor-map copy shared -> global (2-D box at (x, y)), tracked by the
+// issuing thread's bulk groups.  x * element size must be a multiple of 16
+// bytes and x, y non-negative; the source tile is laid out as the map's
+// swizzle mode defines on absolute shared-memory address bits.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(tmap), "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The issuing thread's committed bulk stores have read their shared-memory
+// sources (the sources may be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// The issuing thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Two f32 values to a packed bf16x2 (round to nearest even), `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   uint32_t r;
