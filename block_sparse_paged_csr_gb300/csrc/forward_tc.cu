@@ -7,18 +7,24 @@
 // SMs working at the same time cover neighbouring blocks of one (kv head,
 // sequence) and share its Q rows in L2.  A unit's rows (edge x GQA lane) go
 // through 128-row tiles.  Warp roles, coupled by mbarriers:
-//   warps 1-15 loaders: per unit, the block's K and V rows (through the
-//              block table, f32 or bf16) converted to bf16 once, K as
-//              [keys x 128] and V transposed as [128 x keys], K-major with the
-//              128-byte swizzle (two unit buffers, so the next unit loads
+//   warp 23    scheduler: runs up to four units ahead of the loaders and
+//              resolves each unit's index entries (slot, edge range,
+//              sequence, KV length), its keys' positions and page offsets
+//              through the block table, and the Q row sources of its first
+//              tile into a ring of unit slots, so that the loaders start
+//              every unit with its global addresses at hand;
+//   warps 1-14 loaders: per unit, the block's K and V rows (through the
+//              block table, f32 or bf16) converted to bf16 once, both as
+//              [keys x 128] rows with the 128-byte swizzle: K-major for S,
+//              MN-major for O (two unit buffers, so the next unit loads
 //              while this one computes); per tile, the rows' Q (f32 -> bf16,
-//              same layout) and each row's causal limit (two or three tile
-//              buffers, so the gathers' latency stays off the path);
+//              same layout) (two or three tile buffers, so the gathers'
+//              latency stays off the path);
 //   warp 0     one thread issues S = Q K^T (M=128, N=block, K=128) into TMEM
 //              and, once the softmax has turned S into P, O = P V (M=128,
 //              N=128, K=block; P from TMEM); tcgen05.commit signals the
 //              mbarriers;
-//   warps 16-23 softmax and epilogue, two warpgroups taking alternate tiles
+//   warps 15-22 softmax and epilogue, two warpgroups taking alternate tiles
 //              (and the matching S / O buffer), thread t <-> row t of the
 //              tile (TMEM lane t): S back
 //              with tcgen05.ld, masks (block length, absent pages,
@@ -44,7 +50,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;            // rows per MMA tile
-constexpr int kThreads = 768;   // MMA warp, 15 loader warps, 2 x 4 softmax warps
+constexpr int kThreads = 768;   // MMA warp, 14 loader warps, 2 x 4 softmax warps, scheduler
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // S[2] at columns 0 / 128, O[2] at 256 / 384
@@ -148,10 +154,24 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> f32, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// Shared-memory descriptor of an MN-major operand stored as rows of one K
+// index (128 bytes = 64 MN elements per row, 128-byte swizzle): 8 K rows per
+// swizzle atom (stride 1024 bytes), the next 64 MN elements `lbo` bytes on.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);          // start address
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;       // leading byte offset (MN)
+  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;     // stride byte offset (K)
+  d |= static_cast<uint64_t>(1u) << 46;                         // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                         // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> f32, A K-major, B K-major or (b_mn)
+// MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Byte offset of element pair/quad position inside a K-major, 128B-swizzled
@@ -174,16 +194,18 @@ __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off
   }
 }
 
-constexpr int kLoaders = 15;         // loader warps 1..15
+constexpr int kLoaders = 14;         // loader warps 1..14
 constexpr int kLoadThreads = 32 * kLoaders;
-constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 9
+constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 10
 constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
 
 template <int BS> struct TcCfg {
-  static constexpr int KVB = 2;                   // unit buffers (K, V^T)
+  static constexpr int KVB = 2;                   // unit buffers (K, V)
   static constexpr int NX = BS == 128 ? 2 : 3;    // tile buffers (Q, then P)
 };
 constexpr int kMaxNX = 3;
+constexpr int kRing = 4;                          // unit slots of the scheduler
+constexpr int kSchedWarp = 1 + kLoaders + 8;      // warp 23
 
 struct UnitInfo {
   int32_t rows;         // edges x qhead of the unit (0: skip)
@@ -194,13 +216,25 @@ struct UnitInfo {
   int64_t bstart;       // position of the block's first key
 };
 
-// Shared memory: KVB unit buffers (K, V^T), NX tile buffers (Q), key
-// positions and unit info per unit buffer, key offsets of the unit being
-// loaded, the epilogue's staging tiles, barriers, the TMEM address and
+// Shared memory: KVB unit buffers (K, V), NX tile buffers (Q), key
+// positions and unit info per unit buffer, the scheduler's ring of unit
+// slots, the epilogue's staging tiles, barriers, the TMEM address and
 // per-head unit bases.
 struct TcPlan {
-  size_t kv_bytes;      // one unit buffer: K [BS][128] + V^T [128][BS] bf16
-  size_t kv, x, kpos, info, koff, stage, bars, misc, total;
+  size_t kv_bytes;      // one unit buffer: K [BS][128] + V [BS][128] bf16
+  size_t slot_bytes;    // one unit slot (UnitSlot layout below)
+  size_t kv, x, kpos, info, ring, stage, bars, misc, total;
+};
+
+// A unit slot of the scheduler ring: the unit's info, then per key its
+// source offset in the pool (elements, -1 = no key) and position (-1 = no
+// key), then the Q source offsets (elements, -1 = no row) of the unit's
+// first tile.
+template <int BS> struct SlotLayout {
+  static constexpr size_t koff = 64;                       // int64 [BS]
+  static constexpr size_t kpos = koff + 8 * BS;            // int32 [BS]
+  static constexpr size_t qsrc = kpos + 4 * BS;            // int64 [kM]
+  static constexpr size_t bytes = (qsrc + 8 * 128 + 127) / 128 * 128;
 };
 
 __host__ __device__ constexpr size_t tc_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -217,14 +251,16 @@ __host__ __device__ inline TcPlan tc_plan(int bs) {
   p.x = p.kv + kvb * p.kv_bytes;                                        // [nx] tiles of 32 KB
   p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * 2, 128);     // int32 [kvb][BS]
   p.info = tc_up(p.kpos + kvb * static_cast<size_t>(bs) * 4, 128);      // UnitInfo [kvb]
-  p.koff = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // int64 [BS]
-  p.stage = tc_up(p.koff + static_cast<size_t>(bs) * 8, 1024);          // f32 [8][32][16]
+  p.slot_bytes = bs == 128 ? SlotLayout<128>::bytes : SlotLayout<64>::bytes;
+  p.ring = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // slots [kRing]
+  p.stage = tc_up(p.ring + kRing * p.slot_bytes, 1024);                 // f32 [8][32][16]
   p.bars = tc_up(p.stage + 8 * 32 * 16 * 4, 128);                       // uint64 [32]
   p.misc = tc_up(p.bars + 32 * 8, 128);                                 // TMEM slot, unit bases
   p.total = p.misc + 16 + 201 * 4 + 1024;                               // + alignment slack
   return p;
 }
-static_assert(sizeof(UnitInfo) % 8 == 0, "UnitInfo holds int64 fields");
+static_assert(sizeof(UnitInfo) % 8 == 0 && sizeof(UnitInfo) <= 64, "UnitInfo in a slot header");
+static_assert(4 + 2 * kMaxNX + 10 + 1 + 2 * kRing <= 32, "mbarriers fit their 32 slots");
 
 struct TcBars {
   uint64_t *kv_full, *kv_empty;        // [KVB]
@@ -232,6 +268,7 @@ struct TcBars {
   uint64_t *s_full, *s_free;           // [2] TMEM S buffers
   uint64_t *p_full, *o_full, *o_free;  // [2]
   uint64_t* done;
+  uint64_t *slot_full, *slot_empty;    // [kRing]
 };
 
 // OR of `pred` over the loader warps (named barrier 1); also a barrier.
@@ -256,53 +293,62 @@ __device__ __forceinline__ void unit_head(const int32_t* unit_base, int hkv, int
   j = static_cast<int>(u - unit_base[h]);
 }
 
-// ------------------------------------------------------------------ loaders
+// ------------------------------------------------------------------ scheduler
 
-template <int BS, bool kBf16>
-__device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
-                          const TcBars& B, const int32_t* unit_base, int64_t n_units, int lw,
-                          int lane) {
-  constexpr int KVB = TcCfg<BS>::KVB;
-  constexpr int kNX = TcCfg<BS>::NX;
-  const int lt = lw * 32 + lane;
+// Fills slot U % kRing with unit U of this CTA once the loaders have freed
+// it: the index lookups are spread over lanes so that each level of the
+// chain (slot and edge range, then the sequence's lengths, then the block
+// table and the edges) costs one memory round trip.
+template <int BS>
+__device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
+                             const TcBars& B, const int32_t* unit_base, int64_t n_units,
+                             int lane) {
+  using L = SlotLayout<BS>;
+  constexpr unsigned kAll = 0xffffffffu;
   const int qhead = a.qhead;
   const int ps = a.page_size;
   int64_t* status = a.totals + 3;
-  int64_t* koff = reinterpret_cast<int64_t*>(smem + P.koff);
-  uint32_t U = 0, T = 0;
+  uint32_t U = 0;
   for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
-    const int kvb = static_cast<int>(U % KVB);
-    unsigned char* ks = smem + P.kv + kvb * P.kv_bytes;
-    unsigned char* vs = ks + static_cast<size_t>(BS) * kD * 2;
-    int32_t* kpos = reinterpret_cast<int32_t*>(smem + P.kpos) + kvb * BS;
-    UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + P.info) + kvb;
-    int h, j;
-    unit_head(unit_base, a.hkv, u, h, j);
-    const int raw = a.sel_slots[static_cast<int64_t>(h) * a.nbs + j];
-    const int64_t ebase = a.edge_head_base[h];
-    const int64_t e0 = ebase + a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j];
-    const int64_t e1 = ebase + a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j + 1];
-    const bool bad = raw < 0 || raw >= a.nbs || e1 < e0;
-    if (bad && lt == 0) report(status, SA_ERR_SHAPE);
-    const int b = bad ? 0 : raw / a.msb;
-    const int blk = bad ? 0 : raw - b * a.msb;
-    const int64_t lk = a.used ? max(a.used[b], 0) : static_cast<int64_t>(a.msb) * BS;
-    const int64_t bstart = static_cast<int64_t>(blk) * BS;
-    const int64_t bend = min(bstart + BS, lk);
-    const int64_t q0 = a.cu[b];
-    const int64_t qo = a.cu[b + 1] - q0;
-    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
-
-    bool got = U < static_cast<uint32_t>(KVB) ||
-               mbar_wait_bounded(B.kv_empty + kvb, ((U / KVB) - 1) & 1u);
-    if (loaders_or(!got)) {
-      if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+    const int sl = static_cast<int>(U % kRing);
+    unsigned char* slot = smem + P.ring + sl * P.slot_bytes;
+    const bool got = U < static_cast<uint32_t>(kRing) ||
+                     mbar_wait_bounded(B.slot_empty + sl, ((U / kRing) - 1) & 1u);
+    if (!__all_sync(kAll, got)) {
+      if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
-    // ---- the unit's keys: position (or -1) and source offset ----------------
+    int h, j;
+    unit_head(unit_base, a.hkv, u, h, j);
+    int64_t x = 0;
+    if (lane == 0) x = a.sel_slots[static_cast<int64_t>(h) * a.nbs + j];
+    else if (lane == 1) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j];
+    else if (lane == 2) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j + 1];
+    else if (lane == 3) x = a.edge_head_base[h];
+    const int raw = static_cast<int>(__shfl_sync(kAll, x, 0));
+    const int64_t ebase = __shfl_sync(kAll, x, 3);
+    const int64_t e0 = ebase + __shfl_sync(kAll, x, 1);
+    const int64_t e1 = ebase + __shfl_sync(kAll, x, 2);
+    const bool bad = raw < 0 || raw >= a.nbs || e1 < e0;
+    if (bad && lane == 0) report(status, SA_ERR_SHAPE);
+    const int b = bad ? 0 : raw / a.msb;
+    const int blk = bad ? 0 : raw - b * a.msb;
+    int64_t y = 0;
+    if (lane == 0) y = a.used ? max(a.used[b], 0) : static_cast<int64_t>(a.msb) * BS;
+    else if (lane == 1) y = a.cu[b];
+    else if (lane == 2) y = a.cu[b + 1];
+    const int64_t lk = __shfl_sync(kAll, y, 0);
+    const int64_t q0 = __shfl_sync(kAll, y, 1);
+    const int64_t qo = __shfl_sync(kAll, y, 2) - q0;
+    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
+    const int64_t bstart = static_cast<int64_t>(blk) * BS;
+    const int64_t bend = min(bstart + BS, lk);
+    // the keys: position (or -1) and source offset through the block table
     const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
                         static_cast<int64_t>(blk) * a.pages_per_block;
-    for (int jj = lt; jj < BS; jj += kLoadThreads) {
+    int64_t* koff = reinterpret_cast<int64_t*>(slot + L::koff);
+    int32_t* kpos = reinterpret_cast<int32_t*>(slot + L::kpos);
+    for (int jj = lane; jj < BS; jj += 32) {
       const int64_t pos = bstart + jj;
       int32_t live = -1;
       int64_t off = -1;
@@ -317,61 +363,18 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
       kpos[jj] = live;
       koff[jj] = off;
     }
-    loaders_or(false);   // koff visible to all loaders
-    // K rows: lane = 4 dims, ten of a warp's rows in flight at a time.
-    {
-      constexpr int kRows = (BS + kLoaders - 1) / kLoaders;
-#pragma unroll
-      for (int q0 = 0; q0 < kRows; q0 += 10) {
-        uint2 kr[10];
-#pragma unroll
-        for (int q = 0; q < 10; ++q) {
-          const int r = lw + (q0 + q) * kLoaders;
-          const int64_t off = q0 + q < kRows && r < BS ? koff[r] : -1;
-          kr[q] = off >= 0 ? ld_kv4_bf16<kBf16>(a.k_pages, off + 4 * lane) : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < 10; ++q) {
-          const int r = lw + (q0 + q) * kLoaders;
-          if (q0 + q < kRows && r < BS)
-            *reinterpret_cast<uint2*>(ks + sw128_offset(BS, r, 4 * lane)) = kr[q];
-        }
+    // the first tile's Q sources
+    int64_t* qsrc = reinterpret_cast<int64_t*>(slot + L::qsrc);
+    for (int r = lane; r < kM; r += 32) {
+      int64_t src = -1;
+      if (r < rows) {
+        const int64_t qi = a.edges[2 * (e0 + r / qhead)];
+        src = (qi * a.hq + static_cast<int64_t>(h) * qhead + r % qhead) * kD;
       }
+      qsrc[r] = src;
     }
-    // V^T: a warp takes 8 keys at a time; lane l loads dims 4l..4l+3 of each
-    // key, then writes, for each of its 4 dims d, the 8 keys as one 16-byte
-    // chunk of row d (dim order rotated by lane against bank conflicts).
-    for (int kc = lw; kc < BS / 8; kc += kLoaders) {
-      float4 v[8];
-#pragma unroll
-      for (int uu = 0; uu < 8; ++uu) {
-        const int64_t off = koff[kc * 8 + uu];
-        v[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (off >= 0) {
-          if constexpr (kBf16) {
-            v[uu] = bf16x4_to_f32(__ldg(reinterpret_cast<const uint2*>(
-                static_cast<const uint16_t*>(a.v_pages) + off + 4 * lane)));
-          } else {
-            v[uu] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.v_pages) + off) + lane);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int comp = ((lane >> 1) + i) & 3;
-        float c8[8];
-#pragma unroll
-        for (int uu = 0; uu < 8; ++uu)
-          c8[uu] = comp == 0 ? v[uu].x : comp == 1 ? v[uu].y : comp == 2 ? v[uu].z : v[uu].w;
-        uint4 packed;
-        packed.x = pack_bf16x2_rn(c8[0], c8[1]);
-        packed.y = pack_bf16x2_rn(c8[2], c8[3]);
-        packed.z = pack_bf16x2_rn(c8[4], c8[5]);
-        packed.w = pack_bf16x2_rn(c8[6], c8[7]);
-        *reinterpret_cast<uint4*>(vs + sw128_offset(kD, 4 * lane + comp, kc * 8)) = packed;
-      }
-    }
-    if (lt == 0) {
+    if (lane == 0) {
+      UnitInfo* info = reinterpret_cast<UnitInfo*>(slot);
       info->rows = rows;
       info->h = h;
       info->prow0 = e0 * qhead;
@@ -381,6 +384,76 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
       info->lk = lk;
       info->bstart = bstart;
     }
+    mbar_arrive(B.slot_full + sl);
+  }
+}
+
+// ------------------------------------------------------------------ loaders
+
+template <int BS, bool kBf16>
+__device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
+                          const TcBars& B, const int32_t* unit_base, int64_t n_units, int lw,
+                          int lane) {
+  constexpr int KVB = TcCfg<BS>::KVB;
+  constexpr int kNX = TcCfg<BS>::NX;
+  using L = SlotLayout<BS>;
+  const int lt = lw * 32 + lane;
+  const int qhead = a.qhead;
+  int64_t* status = a.totals + 3;
+  uint32_t U = 0, T = 0;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+    const int kvb = static_cast<int>(U % KVB);
+    unsigned char* ks = smem + P.kv + kvb * P.kv_bytes;
+    unsigned char* vs = ks + static_cast<size_t>(BS) * kD * 2;
+    int32_t* kpos = reinterpret_cast<int32_t*>(smem + P.kpos) + kvb * BS;
+    UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + P.info) + kvb;
+    const int sl = static_cast<int>(U % kRing);
+    const unsigned char* slot = smem + P.ring + sl * P.slot_bytes;
+
+    bool got = mbar_wait_bounded(B.slot_full + sl, (U / kRing) & 1u);
+    got = got && (U < static_cast<uint32_t>(KVB) ||
+                  mbar_wait_bounded(B.kv_empty + kvb, ((U / KVB) - 1) & 1u));
+    if (loaders_or(!got)) {
+      if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    // ---- the unit, as the scheduler resolved it ------------------------------
+    const UnitInfo si = *reinterpret_cast<const UnitInfo*>(slot);
+    const int rows = si.rows;
+    const int h = si.h;
+    const int64_t e0 = si.e0;
+    const int64_t* koff = reinterpret_cast<const int64_t*>(slot + L::koff);
+    const int32_t* skpos = reinterpret_cast<const int32_t*>(slot + L::kpos);
+    for (int jj = lt; jj < BS; jj += kLoadThreads) kpos[jj] = skpos[jj];
+    // K and V rows alike (lane = 4 dims, converted to bf16), ten of a warp's
+    // rows in flight at a time: rows [0, BS) are K, [BS, 2 BS) V, both
+    // stored [key][128] with the 128-byte swizzle (V is the MMA's MN-major B
+    // operand).
+    {
+      constexpr int kRows = (2 * BS + kLoaders - 1) / kLoaders;
+#pragma unroll
+      for (int q0 = 0; q0 < kRows; q0 += 10) {
+        uint2 kr[10];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          const int key = r < BS ? r : r - BS;
+          const int64_t off = q0 + q < kRows && r < 2 * BS ? koff[key] : -1;
+          kr[q] = off >= 0 ? ld_kv4_bf16<kBf16>(r < BS ? a.k_pages : a.v_pages, off + 4 * lane)
+                           : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          if (q0 + q < kRows && r < 2 * BS) {
+            const int key = r < BS ? r : r - BS;
+            *reinterpret_cast<uint2*>((r < BS ? ks : vs) + sw128_offset(BS, key, 4 * lane)) =
+                kr[q];
+          }
+        }
+      }
+    }
+    if (lt == 0) *info = si;
     fence_proxy_async_smem();
     mbar_arrive(B.kv_full + kvb);
 
@@ -398,7 +471,15 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
       }
       return -1;
     };
-    int64_t my_src = row_source(0);
+    // the first tile's sources from the slot, which then goes back to the
+    // scheduler
+    int64_t my_src = -1;
+    {
+      const int r = lw + lane * kLoaders;
+      if (lane < kRowsPerLoader && r < kM)
+        my_src = reinterpret_cast<const int64_t*>(slot + L::qsrc)[r];
+    }
+    mbar_arrive(B.slot_empty + sl);
     for (int rt = 0; rt < rows; rt += kM, ++T) {
       const int xb = static_cast<int>(T % kNX);
       got = T < static_cast<uint32_t>(kNX) ||
@@ -455,12 +536,9 @@ __device__ bool tc_issue_o(unsigned char* smem, const TcPlan& P, const TcBars& B
   const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs) over S's columns
   const uint32_t t_o = tmem + 256 + 128 * sb;
 #pragma unroll
-  for (int st = 0; st < BS / 16; ++st) {
-    const uint32_t panel = st >> 2;
-    const uint32_t kb = (st & 3) * 32;
-    mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc(v_addr + panel * kD * 128 + kb),
-                idesc_bf16(kM, kD), st > 0);
-  }
+  for (int st = 0; st < BS / 16; ++st)   // 16 keys = 2048 bytes of V rows per step
+    mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 2048, BS * 128),
+                idesc_bf16(kM, kD, true), st > 0);
   mma_commit(B.o_full + sb);
   mma_commit(B.s_free + sb);                     // P read: the S / P columns are free
   return true;
@@ -776,6 +854,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   B.o_full = B.s_full + 6;
   B.o_free = B.s_full + 8;
   B.done = B.s_full + 10;
+  B.slot_full = B.done + 1;
+  B.slot_empty = B.slot_full + kRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.misc);
   int32_t* unit_base = reinterpret_cast<int32_t*>(smem + P.misc + 16);   // [hkv + 1]
 
@@ -806,6 +886,10 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
       mbar_init(B.o_free + i, kM);
     }
     mbar_init(B.done, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(B.slot_full + i, 32);
+      mbar_init(B.slot_empty + i, kLoadThreads);
+    }
     fence_mbar_init();
     int32_t acc = 0;
     for (int hh = 0; hh < a.hkv; ++hh) {
@@ -830,10 +914,12 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
     __syncwarp();
   } else if (warp <= kLoaders) {
     tc_loader<BS, kBf16>(a, smem, P, B, unit_base, n_units, warp - 1, lane);
-  } else {
+  } else if (warp < kSchedWarp) {
     tc_softmax<BS>(a, &omap, smem, P, B, tmem, n_units, warp, lane);
     // box stores issued by this thread have landed before the CTA leaves
     bulk_wait_all();
+  } else {
+    tc_scheduler<BS>(a, smem, P, B, unit_base, n_units, lane);
   }
   tc_fence_before();
   __syncthreads();
