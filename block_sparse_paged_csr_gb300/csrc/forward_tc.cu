@@ -201,7 +201,10 @@ constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
 
 template <int BS> struct TcCfg {
   static constexpr int KVB = 2;                   // unit buffers (K, V)
-  static constexpr int NX = BS == 128 ? 2 : 3;    // tile buffers (Q, then P)
+  static constexpr int NX = BS == 128 ? 2 : 3;    // tile buffers (Q)
+  // epilogue staging tiles per warp: two where shared memory allows (the
+  // box store of one drains while the other fills)
+  static constexpr int SB = BS == 128 ? 1 : 2;
 };
 constexpr int kMaxNX = 3;
 constexpr int kRing = 4;                          // unit slots of the scheduler
@@ -245,6 +248,7 @@ __host__ __device__ constexpr size_t tc_up(size_t x, size_t a) { return (x + a -
 __host__ __device__ inline TcPlan tc_plan(int bs) {
   const int kvb = bs == 128 ? TcCfg<128>::KVB : TcCfg<64>::KVB;
   const int nx = bs == 128 ? TcCfg<128>::NX : TcCfg<64>::NX;
+  const int sb = bs == 128 ? TcCfg<128>::SB : TcCfg<64>::SB;
   TcPlan p{};
   p.kv_bytes = static_cast<size_t>(bs) * kD * 2 * 2;
   p.kv = 0;                                                             // 1024-aligned
@@ -253,8 +257,8 @@ __host__ __device__ inline TcPlan tc_plan(int bs) {
   p.info = tc_up(p.kpos + kvb * static_cast<size_t>(bs) * 4, 128);      // UnitInfo [kvb]
   p.slot_bytes = bs == 128 ? SlotLayout<128>::bytes : SlotLayout<64>::bytes;
   p.ring = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // slots [kRing]
-  p.stage = tc_up(p.ring + kRing * p.slot_bytes, 1024);                 // f32 [8][32][16]
-  p.bars = tc_up(p.stage + 8 * 32 * 16 * 4, 128);                       // uint64 [32]
+  p.stage = tc_up(p.ring + kRing * p.slot_bytes, 1024);                 // f32 [8][sb][32][16]
+  p.bars = tc_up(p.stage + 8 * sb * 32 * 16 * 4, 128);                  // uint64 [32]
   p.misc = tc_up(p.bars + 32 * 8, 128);                                 // TMEM slot, unit bases
   p.total = p.misc + 16 + 201 * 4 + 1024;                               // + alignment slack
   return p;
@@ -609,7 +613,11 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
   const int row = (warp & 3) * 32 + lane;               // TMEM lane = tile row
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const float qscale = a.scale * kLog2e;
-  float* wst = reinterpret_cast<float*>(smem + P.stage) + (g * 4 + (warp & 3)) * 32 * 16;
+  // the warp's staging tiles (32 rows x 64 bytes each), used in turn
+  constexpr int SB = TcCfg<BS>::SB;
+  float* const wst0 =
+      reinterpret_cast<float*>(smem + P.stage) + (g * 4 + (warp & 3)) * SB * 32 * 16;
+  uint32_t rnd = 0;
   // The previous tile's row, stored after this tile's softmax.
   bool prev = false;
   uint32_t prevT = 0;
@@ -634,10 +642,20 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
     const int64_t prow0 = __shfl_sync(0xffffffffu, prow, 0);
     const unsigned live = __ballot_sync(0xffffffffu, prow >= 0);
     const bool by_tma = a.o_tma && live == 0xffffffffu;
-    // the staging tile is free once this thread's earlier box stores have
-    // read it (lane 0 issues them)
+    // A round's staging tile is free once the box store last issued from
+    // it has read it: with two tiles, the store of two rounds ago (one box
+    // store per round, issued by lane 0; a round of plain stores waits for
+    // every earlier box store instead); with one, the previous round's.
+    float* wst = wst0;
     auto stage_free = [&]() {
-      if (lane == 0) bulk_wait_read_all();
+      wst = wst0 + (rnd % SB) * 32 * 16;
+      ++rnd;
+      if (lane == 0) {
+        if (SB == 2 && by_tma)
+          bulk_wait_read_1();
+        else
+          bulk_wait_read_all();
+      }
       __syncwarp();
     };
     auto stage_store = [&](int x) {
