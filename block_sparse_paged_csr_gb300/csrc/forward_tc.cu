@@ -601,6 +601,50 @@ __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& 
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+// 2^x by the special-function unit (ex2.approx: relative error about 2^-22;
+// subnormal results flush to zero, below what bf16 P and f32 l resolve).
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of f32 (lo in the low half) and their elementwise a * b + c
+// and a + b, one instruction per pair.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f32x2_split(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Softmax warpgroup g (0 or 1) takes the tiles whose running index has
 // parity g, and with them TMEM buffers S[g], O[g].
 template <int BS>
@@ -778,9 +822,13 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
       }
       tc_fence_after();
       const uint32_t t_s = tmem + 128 * sb + lane_base;
-      // pass 1: the row maximum over live keys (fully live chunks, the common
-      // case, without per-key masks)
-      float m2 = -INFINITY;
+      // pass 1: the row maximum of qscale * s over live keys, as qscale
+      // times the largest (qscale >= 0) or smallest raw score: rounding is
+      // monotonic, so the product is the same maximum (fully live chunks, the
+      // common case, without per-key masks, three scores per instruction)
+      const bool up = qscale >= 0.f;
+      float ext = up ? -INFINITY : INFINITY;
+      bool any = false;
 #pragma unroll 1
       for (int c = 0; c < BS / 32; ++c) {
         float v[32];
@@ -789,19 +837,28 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         const int cut = jlim - c * 32;
         const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
         const uint32_t live = vmask[c] & inside;
+        any = any || live != 0u;
         if (live == 0xffffffffu) {
+          if (up) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) m2 = fmaxf(m2, v[i] * qscale);
+            for (int i = 0; i < 32; i += 2) ext = max3(ext, v[i], v[i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) ext = min3(ext, v[i], v[i + 1]);
+          }
         } else if (live) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if ((live >> i) & 1u) m2 = fmaxf(m2, v[i] * qscale);
+            if ((live >> i) & 1u) ext = up ? fmaxf(ext, v[i]) : fminf(ext, v[i]);
         }
       }
+      const float m2 = any ? ext * qscale : -INFINITY;
       // pass 2: p = exp(s - m), l, and P as bf16 pairs into the S columns
       // already read (chunk c's 16 columns lie at or before S chunk c).
       const float msub = m2 == -INFINITY ? 0.f : m2;
-      float l = 0.f;
+      const uint64_t qs2 = f32x2(qscale, qscale);
+      const uint64_t nm2 = f32x2(-msub, -msub);
+      uint64_t l2 = f32x2(0.f, 0.f);          // two partial sums of p
 #pragma unroll 1
       for (int c = 0; c < BS / 32; ++c) {
         float v[32];
@@ -814,23 +871,30 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         if (live == 0xffffffffu) {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
-            const float p0 = exp2f(fmaf(v[2 * i2], qscale, -msub));
-            const float p1 = exp2f(fmaf(v[2 * i2 + 1], qscale, -msub));
-            l += p0 + p1;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(v[2 * i2], v[2 * i2 + 1]), qs2, nm2), x0, x1);
+            const float p0 = ex2_fast(x0);
+            const float p1 = ex2_fast(x1);
+            l2 = add_f32x2(l2, f32x2(p0, p1));
             pk[i2] = pack_bf16x2_rn(p0, p1);
           }
         } else {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
             const int i = 2 * i2;
-            const float p0 = ((live >> i) & 1u) ? exp2f(fmaf(v[i], qscale, -msub)) : 0.f;
-            const float p1 = ((live >> (i + 1)) & 1u) ? exp2f(fmaf(v[i + 1], qscale, -msub)) : 0.f;
-            l += p0 + p1;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(v[i], v[i + 1]), qs2, nm2), x0, x1);
+            const float p0 = ((live >> i) & 1u) ? ex2_fast(x0) : 0.f;
+            const float p1 = ((live >> (i + 1)) & 1u) ? ex2_fast(x1) : 0.f;
+            l2 = add_f32x2(l2, f32x2(p0, p1));
             pk[i2] = pack_bf16x2_rn(p0, p1);
           }
         }
         tmem_st16(t_s + c * 16, pk);
       }
+      float la, lb;
+      f32x2_split(l2, la, lb);
+      const float l = la + lb;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(B.p_full + sb);
