@@ -337,8 +337,10 @@ def run_ours(args, rank, world, local_rank):
                                   split_edges=split, partials=partials, out=out, lse=lse)
             e[2].record(stream)
         else:
+            # as inside sa_attention: the tensor-core forward keeps a bf16
+            # copy of Q in `out` (written only by the combine)
             sa.sa_forward(q, k, v, index, bt, cu, used, w.hq, w.hkv, w.head_dim, w.block_size,
-                          w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p)
+                          w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p, q_scratch=out)
             e[2].record(stream)
             sa.sa_combine(index, o_p, m_p, l_p, w.hq, w.head_dim, out, lse)
         e[3].record(stream)
@@ -424,7 +426,9 @@ def run_ours(args, rank, world, local_rank):
         "tflops": acct["flops"] / (ms_per_step / 1e3) / 1e12,
         "stages_ms": ({"index": index_ms, "forward_combine": fwd_ms} if fused else
                       {"index": index_ms, "forward": fwd_ms, "combine": comb_ms}),
-        "roofline": {"kernel": f"{fwd_kernel} ({'sa_forward_combine' if fused else 'sa_forward'})",
+        "roofline": {"kernel": f"{fwd_kernel} ({'sa_forward_combine' if fused else 'sa_forward'}"
+                               + (", timed with its Q rounding pass)"
+                                  if fwd_kernel == "forward_tc_kernel" else ")"),
                      "bound": "hbm",
                      "achieved": fwd_gbs, "peak": peak, "unit": "GB/s",
                      "frac": fwd_gbs / peak, "peak_kind": peak_kind,
@@ -435,8 +439,10 @@ def run_ours(args, rank, world, local_rank):
         "edges": acct["edges"],
         "e2e": e2e,
         # library kernels per step: the index kernel, then the fused decode
-        # kernel or forward + combine
-        "gpu_launches": (2 if fused else 3) * args.steps,
+        # kernel, or forward + combine (the tensor-core forward preceded by
+        # the pass that rounds Q to bf16 into its scratch)
+        "gpu_launches": (2 if fused else (4 if fwd_kernel == "forward_tc_kernel" else 3))
+                        * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
         "cpu_baseline": (cpu_baseline(w, args)

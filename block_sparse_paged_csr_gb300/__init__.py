@@ -278,10 +278,13 @@ def partial_rows(index: Index, hq: int) -> int:
 
 def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, used_kv_lens, hq,
                hkv, head_dim, block_size, page_size, softmax_scale, causal, o_partial=None,
-               m_partial=None, l_partial=None, path=PATH_AUTO, stream=None, partial_dtype=None):
+               m_partial=None, l_partial=None, path=PATH_AUTO, stream=None, partial_dtype=None,
+               q_scratch=None):
     """Step 2.  Returns (o_partial, m_partial, l_partial); the first
     totals[0] * qhead rows are valid.  ``partial_dtype="bf16"`` (or a
-    bfloat16 ``o_partial``) stores o in bf16 (sa_forward_ex)."""
+    bfloat16 ``o_partial``) stores o in bf16; ``q_scratch`` (a tensor of at
+    least tq * hq * head_dim * 2 bytes, e.g. the combine's ``out``) lets the
+    tensor-core kernel gather Q from a bf16 copy (both: sa_forward_ex)."""
     _require(q, torch.float32, "q")
     dev = q.device
     kvd = _kv_dtype(k_pages)
@@ -306,8 +309,12 @@ def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, us
             _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), hq, hkv, head_dim,
             block_size, page_size, softmax_scale, int(bool(causal)))
     tail = (_ptr(o_partial), _ptr(m_partial), _ptr(l_partial), path, _stream(stream, dev))
-    if ocode:
-        _check(L.sa_forward_ex(*head, ocode, *tail), "sa_forward_ex")
+    if q_scratch is not None:
+        need = index.c.tq * hq * head_dim * 2
+        if q_scratch.device != dev or q_scratch.numel() * q_scratch.element_size() < need:
+            raise ValueError(f"q_scratch needs {need} bytes on {dev}")
+    if ocode or q_scratch is not None:
+        _check(L.sa_forward_ex(*head, ocode, *tail, _ptr(q_scratch)), "sa_forward_ex")
     else:
         _check(L.sa_forward(*head, *tail), "sa_forward")
     return o_partial, m_partial, l_partial

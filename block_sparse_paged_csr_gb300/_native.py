@@ -88,7 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                i32, i32, f32, i32, p, p, p, st, p]
     lib.sa_forward.restype = st
     lib.sa_forward_ex.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, i32, i32,
-                                  i32, i32, i32, f32, i32, st, p, p, p, st, p]
+                                  i32, i32, i32, f32, i32, st, p, p, p, st, p, p]
     lib.sa_forward_ex.restype = st
     lib.sa_forward_combine.argtypes = [p, p, p, i64, st, ctypes.POINTER(SaIndex), p, p, p, p, p,
                                        i32, i32, i32, i32, f32, i32, i32, p, p, p, p, p, st, p]

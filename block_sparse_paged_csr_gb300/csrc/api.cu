@@ -226,13 +226,19 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-sa_status sa_forward_ex(const float* q, const void* k_pages, const void* v_pages,
-                        int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
-                        const int32_t* block_tables, const int64_t* cu_seqlens_q,
-                        const int32_t* used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
-                        int32_t block_size, int32_t page_size, float softmax_scale,
-                        int32_t causal, sa_dtype partial_dtype, void* o_partial,
-                        float* m_partial, float* l_partial, sa_path path, void* stream) {
+namespace {
+
+// Step 2.  `q16_scratch` (nullable): room for tq * hq * head_dim bf16 values,
+// 16-byte aligned, not overlapping q, that the tensor-core kernel may fill
+// with Q rounded to bf16 and gather from (half the bytes of the f32 rows, no
+// conversion per gather); its content afterwards is unspecified.
+sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
+                       int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                       const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                       const int32_t* used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
+                       int32_t block_size, int32_t page_size, float softmax_scale, int32_t causal,
+                       sa_dtype partial_dtype, void* o_partial, float* m_partial,
+                       float* l_partial, sa_path path, void* stream, void* q16_scratch) {
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0) return SA_ERR_HEAD_COUNT;
   if (head_dim <= 0 || block_size <= 0 || page_size <= 0 || block_size % page_size != 0)
     return SA_ERR_BLOCK_PAGE;
@@ -294,6 +300,12 @@ sa_status sa_forward_ex(const float* q, const void* k_pages, const void* v_pages
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
+  if (kernel == FwdKernel::kTensor && q16_scratch != nullptr) {
+    const int64_t n = idx->tq * static_cast<int64_t>(hq) * head_dim;
+    err = sa::launch_q_to_bf16(q, static_cast<uint16_t*>(q16_scratch), n, s);
+    if (err != cudaSuccess) return SA_ERR_CUDA;
+    a.q16 = static_cast<const uint16_t*>(q16_scratch);
+  }
   switch (kernel) {
     case FwdKernel::kDecodeMma: err = sa::launch_forward_dec_mma(a, s); break;
     case FwdKernel::kTensor: err = sa::launch_forward_tc(a, s); break;
@@ -304,6 +316,34 @@ sa_status sa_forward_ex(const float* q, const void* k_pages, const void* v_pages
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+sa_status sa_forward_ex(const float* q, const void* k_pages, const void* v_pages,
+                        int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                        const int32_t* block_tables, const int64_t* cu_seqlens_q,
+                        const int32_t* used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
+                        int32_t block_size, int32_t page_size, float softmax_scale,
+                        int32_t causal, sa_dtype partial_dtype, void* o_partial,
+                        float* m_partial, float* l_partial, sa_path path, void* stream,
+                        void* q_scratch) {
+  if (q_scratch != nullptr) {
+    const size_t qbytes = idx ? static_cast<size_t>(idx->tq) * (hq > 0 ? hq : 0) *
+                                    (head_dim > 0 ? head_dim : 0) * sizeof(float)
+                              : 0;
+    if (!aligned16(q_scratch) || head_dim % 8 != 0 || overlaps(q, qbytes, q_scratch, qbytes / 2))
+      return SA_ERR_INVALID_ARGUMENT;
+  }
+  return forward_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables, cu_seqlens_q,
+                      used_kv_lens, hq, hkv, head_dim, block_size, page_size, softmax_scale,
+                      causal, partial_dtype, o_partial, m_partial, l_partial, path, stream,
+                      q_scratch);
+}
+
 sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, int64_t num_pages,
                      sa_dtype kv_dtype, const sa_index* idx, const int32_t* block_tables,
                      const int64_t* cu_seqlens_q, const int32_t* used_kv_lens, int32_t hq,
@@ -312,7 +352,8 @@ sa_status sa_forward(const float* q, const void* k_pages, const void* v_pages, i
                      float* l_partial, sa_path path, void* stream) {
   return sa_forward_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx, block_tables, cu_seqlens_q,
                        used_kv_lens, hq, hkv, head_dim, block_size, page_size, softmax_scale,
-                       causal, SA_DTYPE_F32, o_partial, m_partial, l_partial, path, stream);
+                       causal, SA_DTYPE_F32, o_partial, m_partial, l_partial, path, stream,
+                       nullptr);
 }
 
 const char* sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_t hkv,
@@ -411,11 +452,19 @@ sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void*
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
   }
   if (!fused) {
-    const sa_status st = sa_forward_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx,
-                                       block_tables, cu_seqlens_q, used_kv_lens, hq, hkv,
-                                       head_dim, block_size, page_size, softmax_scale, causal,
-                                       partial_dtype, o_partial, m_partial, l_partial, path,
-                                       stream);
+    // `out` is not written before the combine: the tensor-core forward may
+    // keep a bf16 copy of Q there (in its first half), unless out and q
+    // share memory.
+    const size_t qbytes = static_cast<size_t>(tq) * hq * head_dim * sizeof(float);
+    void* q16 = (out != nullptr && q != nullptr && qbytes > 0 && head_dim % 8 == 0 &&
+                 aligned16(out) && !overlaps(q, qbytes, out, qbytes))
+                    ? static_cast<void*>(out)
+                    : nullptr;
+    const sa_status st = forward_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx,
+                                      block_tables, cu_seqlens_q, used_kv_lens, hq, hkv, head_dim,
+                                      block_size, page_size, softmax_scale, causal,
+                                      partial_dtype, o_partial, m_partial, l_partial, path,
+                                      stream, q16);
     if (st != SA_OK) return st;
     return sa_combine_ex(idx, partial_dtype, o_partial, m_partial, l_partial, hq, head_dim, out,
                          lse, stream);

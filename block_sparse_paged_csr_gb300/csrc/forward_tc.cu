@@ -494,30 +494,62 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
       }
       unsigned char* xq = smem + P.x + static_cast<size_t>(xb) * kM * kD * 2;
       int64_t nxt_src = -1;
+      if (a.q16 != nullptr) {
+        // bf16 rows (256 bytes): a half-warp per row, 8 dims per lane, two
+        // of the warp's rows per load instruction
+        constexpr int kPairs = (kRowsPerLoader + 1) / 2;
+        const int hl = lane & 15;
+        const int half = lane >> 4;
+        uint4 w[kPairs];
 #pragma unroll
-      for (int q0 = 0; q0 < kRowsPerLoader; q0 += kQBatch) {
-        float4 v[kQBatch];
-#pragma unroll
-        for (int q = 0; q < kQBatch; ++q) {
-          const int64_t src = __shfl_sync(0xffffffffu, my_src, (q0 + q) & 31);
-          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (q0 + q < kRowsPerLoader && src >= 0)
-            v[q] = __ldg(reinterpret_cast<const float4*>(a.q + src) + lane);
+        for (int i = 0; i < kPairs; ++i) {
+          const int q = 2 * i + half;
+          const int64_t src = __shfl_sync(0xffffffffu, my_src, q & 31);
+          w[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (q < kRowsPerLoader && src >= 0)
+            w[i] = __ldg(reinterpret_cast<const uint4*>(a.q16 + src) + hl);
         }
-        if (q0 == 0 && rt + kM < rows) {
+        if (rt + kM < rows) {
           nxt_src = row_source(rt + kM);
-          // the next tile's rows start for L2 now; their loads come a tile later
           if (nxt_src >= 0)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.q + nxt_src),
-                         "r"(static_cast<uint32_t>(kD * 4))
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.q16 + nxt_src),
+                         "r"(static_cast<uint32_t>(kD * 2))
                          : "memory");
         }
 #pragma unroll
-        for (int q = 0; q < kQBatch; ++q) {
-          const int r = lw + (q0 + q) * kLoaders;
-          if (q0 + q < kRowsPerLoader && r < kM)
-            *reinterpret_cast<uint2*>(xq + sw128_offset(kM, r, 4 * lane)) =
-                make_uint2(pack_bf16x2_rn(v[q].x, v[q].y), pack_bf16x2_rn(v[q].z, v[q].w));
+        for (int i = 0; i < kPairs; ++i) {
+          const int q = 2 * i + half;
+          const int r = lw + q * kLoaders;
+          if (q < kRowsPerLoader && r < kM)
+            *reinterpret_cast<uint4*>(xq + sw128_offset(kM, r, 8 * hl)) = w[i];
+        }
+      } else {
+        // f32 rows (512 bytes): lane = 4 dims, converted to bf16
+#pragma unroll
+        for (int q0 = 0; q0 < kRowsPerLoader; q0 += kQBatch) {
+          float4 v[kQBatch];
+#pragma unroll
+          for (int q = 0; q < kQBatch; ++q) {
+            const int64_t src = __shfl_sync(0xffffffffu, my_src, (q0 + q) & 31);
+            v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q0 + q < kRowsPerLoader && src >= 0)
+              v[q] = __ldg(reinterpret_cast<const float4*>(a.q + src) + lane);
+          }
+          if (q0 == 0 && rt + kM < rows) {
+            nxt_src = row_source(rt + kM);
+            // the next tile's rows start for L2 now; their loads come a tile later
+            if (nxt_src >= 0)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.q + nxt_src),
+                           "r"(static_cast<uint32_t>(kD * 4))
+                           : "memory");
+          }
+#pragma unroll
+          for (int q = 0; q < kQBatch; ++q) {
+            const int r = lw + (q0 + q) * kLoaders;
+            if (q0 + q < kRowsPerLoader && r < kM)
+              *reinterpret_cast<uint2*>(xq + sw128_offset(kM, r, 4 * lane)) =
+                  make_uint2(pack_bf16x2_rn(v[q].x, v[q].y), pack_bf16x2_rn(v[q].z, v[q].w));
+          }
         }
       }
       fence_proxy_async_smem();
@@ -1050,6 +1082,33 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace {
+
+__global__ void __launch_bounds__(256) q_to_bf16_kernel(const float4* __restrict__ q,
+                                                        uint4* __restrict__ q16, int64_t n8) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 x = q[2 * i];
+    const float4 y = q[2 * i + 1];
+    q16[i] = make_uint4(pack_bf16x2_rn(x.x, x.y), pack_bf16x2_rn(x.z, x.w),
+                        pack_bf16x2_rn(y.x, y.y), pack_bf16x2_rn(y.z, y.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_q_to_bf16(const float* q, uint16_t* q16, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const int64_t n8 = n / 8;
+  int64_t grid = static_cast<int64_t>(device_sm_count()) * 8;
+  const int64_t need = (n8 + 255) / 256;
+  if (grid > need) grid = need;
+  q_to_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(q), reinterpret_cast<uint4*>(q16), n8);
+  return cudaGetLastError();
+}
 
 bool forward_tc_supported(int head_dim, int block_size, int page_size, int qhead) {
   if (head_dim != kD) return false;

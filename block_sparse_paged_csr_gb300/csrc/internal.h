@@ -73,6 +73,7 @@ struct ForwardArgs {
   void* o_partial;          // f32, or bf16 when o_bf16
   int o_bf16;
   int o_tma;                // set by a launcher: o rows may go out by tensor-map stores
+  const uint16_t* q16;      // nullable: Q rounded to bf16, same layout (tensor-core kernel)
   float* m_partial;
   float* l_partial;
 };
@@ -83,6 +84,9 @@ bool forward_cc_supported(int head_dim, int block_size, int kv_bf16);
 
 // Tensor-core (tcgen05) forward for units with many gathered rows.
 cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t stream);
+// q [n] f32 -> q16 [n] bf16 (round to nearest even); n a multiple of 8,
+// both 16-byte aligned.
+cudaError_t launch_q_to_bf16(const float* q, uint16_t* q16, int64_t n, cudaStream_t stream);
 bool forward_tc_supported(int head_dim, int block_size, int page_size, int qhead);
 
 // Decode-shaped forward with bf16 K/V on warp-level tensor-core MMA.

@@ -263,6 +263,15 @@ sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
  * writes and the combine reads, at a relative error of at most 2^-8 per o
  * value before the combine.  Every forward kernel supports it.  Other
  * partial_dtype values: SA_ERR_INVALID_ARGUMENT.
+ *
+ * q_scratch (nullable): device memory of tq * hq * head_dim * 2 bytes,
+ * 16-byte aligned, not overlapping q (head_dim a multiple of 8), which the
+ * tensor-core kernel may fill with Q rounded to bf16 (one extra pass over Q)
+ * and gather its tiles from; the result is identical (that kernel rounds Q
+ * to bf16 either way) and the scratch content afterwards unspecified.
+ * sa_forward_combine and sa_attention pass the first half of `out` (written
+ * only by the combine) unless out and q overlap.  Bad scratch:
+ * SA_ERR_INVALID_ARGUMENT.
  */
 sa_status sa_forward_ex(const float *q, const void *k_pages, const void *v_pages,
                         int64_t num_pages, sa_dtype kv_dtype, const sa_index *idx,
@@ -270,7 +279,8 @@ sa_status sa_forward_ex(const float *q, const void *k_pages, const void *v_pages
                         const int32_t *used_kv_lens, int32_t hq, int32_t hkv, int32_t head_dim,
                         int32_t block_size, int32_t page_size, float softmax_scale,
                         int32_t causal, sa_dtype partial_dtype, void *o_partial,
-                        float *m_partial, float *l_partial, sa_path path, void *stream);
+                        float *m_partial, float *l_partial, sa_path path, void *stream,
+                        void *q_scratch);
 
 /*
  * Name of the kernel sa_forward launches for a problem of tq queries in

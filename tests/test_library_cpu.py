@@ -132,13 +132,18 @@ def test_partial_dtype_host_checks(lib):
 
     def fwd(pdt, hq=4, d=32):
         return lib.sa_forward_ex(None, None, None, 16, 0, ctypes.byref(idx), None, None, None, hq,
-                                 2, d, 32, 16, 0.1, 0, pdt, None, None, None, 0, None)
+                                 2, d, 32, 16, 0.1, 0, pdt, None, None, None, 0, None, None)
 
     assert fwd(2) == names["INVALID_ARGUMENT"]
     assert fwd(-1) == names["INVALID_ARGUMENT"]
     assert fwd(1, hq=3) == names["HEAD_COUNT"]
     assert fwd(1, d=30) == names["UNSUPPORTED"]
     assert fwd(1) == names["INVALID_ARGUMENT"]       # null pointers
+    # a Q scratch that is misaligned, or overlaps q, is refused before any launch
+    q = ctypes.c_void_p(4096)
+    for scratch in (ctypes.c_void_p(4104), ctypes.c_void_p(4096 + 64)):
+        assert lib.sa_forward_ex(q, q, q, 16, 0, ctypes.byref(idx), q, q, None, 4, 2, 32, 32, 16,
+                                 0.1, 0, 0, q, q, q, 0, None, scratch) == names["INVALID_ARGUMENT"]
     comb = lib.sa_combine_ex
     assert comb(ctypes.byref(idx), 2, None, None, None, 4, 32, None, None, None) == \
         names["INVALID_ARGUMENT"]

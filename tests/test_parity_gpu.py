@@ -277,3 +277,29 @@ def test_decode_mma_shapes(bs, ps, qhead):
     w.block_tables[2, 1] = -1
     w.selected[3, 1, 2] = w.selected[3, 1, 1]      # a block selected at two ranks
     _check_against_oracle(w, _gpu.device_workload(w), 0, sa.PATH_TENSOR_CORE, _gpu.TOL_F32)
+
+
+@pytest.mark.parametrize("name", ["chunked_prefill", "chunked_prefill_bf16", "skewed"])
+def test_tensor_core_bf16_q_copy_matches_f32_gather(name):
+    """sa_attention lets the tensor-core forward gather Q from a bf16 copy it
+    keeps in `out` until the combine; sa_forward gathers the f32 rows and
+    rounds them itself.  Same rounding, so the partials are bit-identical;
+    and an `out` that is q itself (no room for the copy) gives the same
+    output."""
+    w = inputs.small(name, seed=9)
+    t = _gpu.device_workload(w)
+    out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=3, path=sa.PATH_TENSOR_CORE)
+    o2, m2, l2 = sa.sa_forward(t["q"], t["k"], t["v"], idx, t["bt"], t["cu"], t["used"], w.hq,
+                               w.hkv, w.head_dim, w.block_size, w.page_size, w.softmax_scale,
+                               w.causal, path=sa.PATH_TENSOR_CORE)
+    assert sa.sa_get_status(idx) == 0
+    rows = int(idx.to_host()["edges"].shape[0]) * w.qhead
+    assert torch.equal(o[:rows], o2[:rows])
+    assert torch.equal(m[:rows], m2[:rows]) and torch.equal(l[:rows], l2[:rows])
+    q_alias = t["q"].clone()
+    out3, lse3, _, _ = sa.sa_attention(q_alias, t["k"], t["v"], t["selected"], w.cu_seqlens_q,
+                                       t["cu"], t["used"], t["bt"], w.hq, w.hkv, w.head_dim,
+                                       w.block_size, w.page_size, w.softmax_scale, w.causal,
+                                       split_edges=3, out=q_alias, path=sa.PATH_TENSOR_CORE)
+    torch.cuda.synchronize()
+    assert torch.equal(out3, out) and torch.equal(lse3, lse)
