@@ -72,6 +72,14 @@ def make_workload(name: str, seed: int):
         w = inputs.chunked_prefill(seed, batch=1)
         w.name = name
         return w
+    if name == "chunked_prefill_bf16_ncu":
+        w = inputs.chunked_prefill(seed, batch=1, kv_dtype="bf16")
+        w.name = name
+        return w
+    if name == "skewed_ncu":
+        w = inputs.skewed(seed, batch=4)
+        w.name = name
+        return w
     if name == "long_decode_ncu":
         w = inputs.long_decode(seed, batch=128, kv_min=8192, kv_max=12288)
         w.name = name
