@@ -1086,6 +1086,23 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
 
 // ------------------------------------------------------------------ host
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
 
 // K or V pool [num_pages, hkv, page_size, 128] as rows of one key.
 //   f32:  3-D (32 floats, 4 quarters, rows), box (32, 4, kb);
@@ -1161,19 +1178,6 @@ cudaError_t launch_fused(const FusedDecArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
 
 bool fused_dec_supported(int head_dim, int block_size, int page_size, int qhead, int kv_bf16) {
   if (head_dim != kD) return false;
