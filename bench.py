@@ -270,7 +270,8 @@ def run_ours(args, rank, world, local_rank):
     w = make_workload(args.workload, args.seed + rank)
     split = SPLIT_EDGES.get(args.workload.replace("_ncu", ""), 0)
     fwd_kernel = sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq,
-                                             w.head_dim, w.block_size, w.page_size, w.kv_dtype)
+                                             w.head_dim, w.block_size, w.page_size, w.kv_dtype,
+                                             causal=w.causal)
     fused = fwd_kernel == "fused_dec_kernel"
     acct = algorithmic_bytes(w, fused, o_bytes=2 if args.partials == "bf16" else 4)
 

@@ -33,7 +33,7 @@ __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
            "sa_attention_kernel_name", "PATH_FUSED_DECODE",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
-           "PATH_CUDA_CORE_GENERAL"]
+           "PATH_CUDA_CORE_GENERAL", "AttentionGraph"]
 
 
 class SAError(RuntimeError):
@@ -44,6 +44,17 @@ class SAError(RuntimeError):
         self.kind = STATUS_NAMES.get(self.code, f"UNKNOWN({code})")
         text = _native.load().sa_status_string(self.code).decode()
         super().__init__(f"{where}: {self.kind} ({text})")
+
+
+def _causal(causal) -> int:
+    """The C ABI's causal mode: 0 none, 1 right-aligned (the pages' rule), 2
+    left-aligned (opt-in); booleans map to 0 / 1."""
+    if isinstance(causal, (bool, np.bool_)):
+        return int(causal)
+    c = int(causal)
+    if c not in (0, 1, 2):
+        raise ValueError(f"causal must be 0, 1 or 2, got {causal!r}")
+    return c
 
 
 def _check(code: int, where: str) -> None:
@@ -238,14 +249,14 @@ def sa_forward_kernel_name(tq, batch, hkv, hq, head_dim, block_size, page_size, 
 
 
 def sa_attention_kernel_name(cu_seqlens_q_host, num_pages, hkv, hq, head_dim, block_size,
-                             page_size, kv_dtype="f32", path=PATH_AUTO):
+                             page_size, kv_dtype="f32", path=PATH_AUTO, causal=0):
     """The kernel sa_attention runs for steps 2 and 3 ("fused_dec_kernel" on
-    the fused decode path), or None where it would refuse the shape."""
+    the fused decode path), or None where it would refuse the call."""
     cu = _host_i64(cu_seqlens_q_host)
     dt = {"f32": DTYPE_F32, "bf16": DTYPE_BF16}[kv_dtype]
     name = _native.load().sa_attention_kernel_name(
         int(cu[-1]), len(cu) - 1, cu.ctypes.data, int(num_pages), hq, hkv, head_dim, block_size,
-        page_size, dt, int(path))
+        page_size, dt, _causal(causal), int(path))
     return None if name is None else name.decode()
 
 
@@ -307,7 +318,7 @@ def sa_forward(q, k_pages, v_pages, index: Index, block_tables, cu_seqlens_q, us
     L = _native.load()
     head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(index.c),
             _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(used_kv_lens), hq, hkv, head_dim,
-            block_size, page_size, softmax_scale, int(bool(causal)))
+            block_size, page_size, softmax_scale, _causal(causal))
     tail = (_ptr(o_partial), _ptr(m_partial), _ptr(l_partial), path, _stream(stream, dev))
     if q_scratch is not None:
         need = index.c.tq * hq * head_dim * 2
@@ -371,7 +382,7 @@ def sa_forward_combine(q, k_pages, v_pages, index: Index, selected, cu_seqlens_q
     head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, ctypes.byref(c),
             _ptr(selected), cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q),
             _ptr(used_kv_lens), _ptr(block_tables), hq, head_dim, block_size, page_size,
-            softmax_scale, int(bool(causal)), split_edges)
+            softmax_scale, _causal(causal), split_edges)
     tail = (_ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path, _stream(stream, dev))
     if ocode:
         _check(L.sa_forward_combine_ex(*head, ocode, *tail), "sa_forward_combine_ex")
@@ -415,13 +426,49 @@ def sa_attention(q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q,
     head = (_ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages, kvd, _ptr(selected), tq, topk,
             cu_h.ctypes.data_as(ctypes.c_void_p), _ptr(cu_seqlens_q), batch, _ptr(used_kv_lens),
             _ptr(block_tables), max_pages, hq, hkv, head_dim, block_size, page_size,
-            softmax_scale, int(bool(causal)), split_edges, ctypes.byref(index.c))
+            softmax_scale, _causal(causal), split_edges, ctypes.byref(index.c))
     tail = (_ptr(o), _ptr(m), _ptr(l), _ptr(out), _ptr(lse), path, _stream(stream, dev))
     if ocode:
         _check(L.sa_attention_ex(*head, ocode, *tail), "sa_attention_ex")
     else:
         _check(L.sa_attention(*head, *tail), "sa_attention")
     return out, lse, index, partials
+
+
+class AttentionGraph:
+    """Steps 1-3 (sa_attention) captured once into a CUDA graph on fixed
+    buffers and replayed: for small decode batches, where the launches of
+    the index, forward and combine kernels cost as much as their work.
+
+    Every argument is bound at capture: the device tensors by address (their
+    contents may change between replays: new queries, selections, block
+    tables, lengths) and the host-side facts the library decides on at call
+    time (cu_seqlens_q_host, head counts, sizes, path), which must then stay
+    what they were.  ``replay()`` enqueues the graph on the current stream
+    and returns (out, lse); status checks go through ``sa_get_status(self.index)``.
+    """
+
+    def __init__(self, q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q,
+                 used_kv_lens, block_tables, hq, hkv, head_dim, block_size, page_size,
+                 softmax_scale, causal, split_edges=0, path=PATH_AUTO, partial_dtype=None):
+        args = (q, k_pages, v_pages, selected, cu_seqlens_q_host, cu_seqlens_q, used_kv_lens,
+                block_tables, hq, hkv, head_dim, block_size, page_size, softmax_scale, causal)
+        kw = dict(split_edges=split_edges, path=path)
+        # one eager call first: buffers, library load and kernel attributes
+        self.out, self.lse, self.index, self.partials = sa_attention(
+            *args, partial_dtype=partial_dtype, **kw)
+        torch.cuda.synchronize(q.device)
+        status = sa_get_status(self.index)
+        if status != 0:
+            raise SAError(status, "AttentionGraph (eager call)")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            sa_attention(*args, index=self.index, partials=self.partials, out=self.out,
+                         lse=self.lse, **kw)
+
+    def replay(self):
+        self.graph.replay()
+        return self.out, self.lse
 
 
 def sa_get_status(index: Index, stream=None) -> int:

@@ -99,7 +99,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_forward_combine_ex.restype = st
     lib.sa_forward_kernel_name.argtypes = [i64, i32, i32, i32, i32, i32, i32, st, st]
     lib.sa_forward_kernel_name.restype = ctypes.c_char_p
-    lib.sa_attention_kernel_name.argtypes = [i64, i32, p, i64, i32, i32, i32, i32, i32, st, st]
+    lib.sa_attention_kernel_name.argtypes = [i64, i32, p, i64, i32, i32, i32, i32, i32, st, i32,
+                                             st]
     lib.sa_attention_kernel_name.restype = ctypes.c_char_p
     lib.sa_combine.argtypes = [ctypes.POINTER(SaIndex), p, p, p, i32, i32, p, p, p]
     lib.sa_combine.restype = st

@@ -263,6 +263,7 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
     return SA_ERR_INVALID_ARGUMENT;
+  if (causal < 0 || causal > 2) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   if (path == SA_PATH_FUSED_DECODE) return SA_ERR_UNSUPPORTED;   // writes no partials
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
@@ -297,7 +298,7 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   a.msb = idx->msb;
   a.nbs = idx->nbs;
   a.scale = softmax_scale;
-  a.causal = causal != 0;
+  a.causal = causal;
   a.sel_slots = idx->sel_slots;
   a.sel_offsets = idx->sel_offsets;
   a.num_sel = idx->num_sel;
@@ -383,18 +384,19 @@ const char* sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_
 const char* sa_attention_kernel_name(int64_t tq, int32_t batch, const int64_t* cu_seqlens_q_host,
                                      int64_t num_pages, int32_t hq, int32_t hkv,
                                      int32_t head_dim, int32_t block_size, int32_t page_size,
-                                     sa_dtype kv_dtype, sa_path path) {
+                                     sa_dtype kv_dtype, int32_t causal, sa_path path) {
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return nullptr;
+  if (causal < 0 || causal > 2) return nullptr;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
-  if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
+  if ((path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) && causal != 2) {
     if (hkv > 0 && hq > 0 && hq % hkv == 0 && head_dim > 0 && block_size > 0 && page_size > 0 &&
         block_size % page_size == 0 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK &&
         cu_seqlens_q_host[batch] == tq &&
         fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim, block_size,
                        page_size, kv_bf16))
       return "fused_dec_kernel";
-    if (path == SA_PATH_FUSED_DECODE) return nullptr;
   }
+  if (path == SA_PATH_FUSED_DECODE) return nullptr;
   return sa_forward_kernel_name(tq, batch, hq, hkv, head_dim, block_size, page_size, kv_dtype,
                                 path);
 }
@@ -454,12 +456,15 @@ sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void*
   if (idx->block_size != block_size || idx->page_size != page_size) return SA_ERR_SHAPE;
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   if (split_edges < 0) return SA_ERR_INVALID_ARGUMENT;
+  if (causal < 0 || causal > 2) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   const int64_t tq = idx->tq;
   const int32_t batch = idx->batch;
   bool fused = false;
   if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
-    if (validate_cu_host(cu_seqlens_q_host, batch) == SA_OK && cu_seqlens_q_host[batch] == tq)
+    // (left-aligned causal masks a lone query's keys: not the fused path's case)
+    if (causal != 2 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK &&
+        cu_seqlens_q_host[batch] == tq)
       fused = fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim,
                              block_size, page_size, kv_bf16);
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
@@ -581,11 +586,12 @@ sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pag
   if (kv_dtype != SA_DTYPE_F32 && kv_dtype != SA_DTYPE_BF16) return SA_ERR_INVALID_ARGUMENT;
   if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
     return SA_ERR_INVALID_ARGUMENT;
+  if (causal < 0 || causal > 2) return SA_ERR_INVALID_ARGUMENT;
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   // Shape checks of the forward step, before any device work.
   bool fused = false;
   if (path == SA_PATH_AUTO || path == SA_PATH_FUSED_DECODE) {
-    if (tq > 0 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK)
+    if (causal != 2 && tq > 0 && validate_cu_host(cu_seqlens_q_host, batch) == SA_OK)
       fused = fused_eligible(tq, batch, cu_seqlens_q_host, num_pages, hq, hkv, head_dim,
                              block_size, page_size, kv_bf16);
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;

@@ -195,7 +195,7 @@ forward_cc_kernel(ForwardArgs a) {
           int64_t lim = INT32_MAX;
           if (a.causal) {
             const int64_t ql = qi - q0;
-            lim = lk >= qo ? lk - qo + ql : ql;
+            lim = a.causal == 2 || lk < qo ? ql : lk - qo + ql;
           }
           rlim[r] = static_cast<int32_t>(lim < INT32_MAX ? lim : INT32_MAX);
         }

@@ -218,7 +218,7 @@ forward_dec_mma_kernel(ForwardArgs a) {
             int64_t l64 = INT32_MAX;
             if (a.causal) {
               const int64_t ql = qidx - m.q0;
-              l64 = m.lk >= m.qo ? m.lk - m.qo + ql : ql;
+              l64 = a.causal == 2 || m.lk < m.qo ? ql : m.lk - m.qo + ql;
             }
             lim[h2] = static_cast<int>(l64 < INT32_MAX ? l64 : INT32_MAX);
           }

@@ -842,7 +842,7 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
           const int rr = tt * kM + row;
           const int64_t qi = a.edges[2 * (info.e0 + rr / a.qhead)];
           const int64_t ql = qi - info.q0;
-          const int64_t lim = info.lk >= info.qo ? info.lk - info.qo + ql : ql;
+          const int64_t lim = a.causal == 2 || info.lk < info.qo ? ql : info.lk - info.qo + ql;
           const int64_t rel = lim - info.bstart;
           jlim = rel < -1 ? -1 : (rel > BS - 1 ? BS - 1 : static_cast<int>(rel));
         }

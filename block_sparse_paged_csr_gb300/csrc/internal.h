@@ -59,7 +59,7 @@ struct ForwardArgs {
   int32_t hq, hkv, qhead, head_dim, block_size, page_size, pages_per_block, max_pages, msb;
   int64_t nbs;
   float scale;
-  int causal;
+  int causal;               // 0 none, 1 right-aligned, 2 left-aligned
   // index
   const int32_t* sel_slots;
   const int32_t* sel_offsets;

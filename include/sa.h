@@ -224,9 +224,12 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  *                 kept block's live range are read
  *   cu_seqlens_q, used_kv_lens  as for sa_build_index (device)
  *   softmax_scale scores are softmax_scale * <q, k>
- *   causal        nonzero: key at absolute position p is live for query i of
+ *   causal        1: key at absolute position p is live for query i of
  *                 sequence b iff p <= lk_b - qo_b + (i - cu[b]) when
- *                 lk_b >= qo_b, else p <= i - cu[b] (right-aligned)
+ *                 lk_b >= qo_b, else p <= i - cu[b] (right-aligned, the rule
+ *                 of forward.rs); 2: iff p <= i - cu[b] (left-aligned, the
+ *                 forward.rs doc's reading for unknown KV lengths, an
+ *                 opt-in); 0: no mask; other values SA_ERR_INVALID_ARGUMENT
  *   o_partial     [tq*hkv*topk*qhead, head_dim] float32; rows e*qhead + qh
  *   m_partial,
  *   l_partial     [tq*hkv*topk*qhead] float32
@@ -296,15 +299,15 @@ const char *sa_forward_kernel_name(int64_t tq, int32_t batch, int32_t hq, int32_
                                    sa_dtype kv_dtype, sa_path path);
 
 /*
- * The kernel that sa_attention / sa_forward_combine run for steps 2 and 3:
- * "fused_dec_kernel" on the fused decode path (see sa_attention), else the
- * name sa_forward_kernel_name gives; NULL where the shape would be refused.
- * Host only (reads cu_seqlens_q_host[0..batch]).
+ * The kernel that sa_attention / sa_forward_combine run for steps 2 and 3
+ * with this `causal` mode: "fused_dec_kernel" on the fused decode path (see
+ * sa_attention), else the name sa_forward_kernel_name gives; NULL where the
+ * call would be refused.  Host only (reads cu_seqlens_q_host[0..batch]).
  */
 const char *sa_attention_kernel_name(int64_t tq, int32_t batch, const int64_t *cu_seqlens_q_host,
                                      int64_t num_pages, int32_t hq, int32_t hkv,
                                      int32_t head_dim, int32_t block_size, int32_t page_size,
-                                     sa_dtype kv_dtype, sa_path path);
+                                     sa_dtype kv_dtype, int32_t causal, sa_path path);
 
 /*
  * Steps 2 and 3 on an index built by sa_build_index (same stream), with no
@@ -365,8 +368,9 @@ sa_status sa_combine_ex(const sa_index *idx, sa_dtype partial_dtype, const void 
  * caller's index arrays and workspace and is filled in as by sa_build_index.
  * The partial buffers are scratch of the sizes sa_forward documents.
  *
- * Fused decode path (SA_PATH_AUTO or SA_PATH_FUSED_DECODE): when every
- * sequence holds at most one query (cu_seqlens_q_host), head_dim is 128,
+ * Fused decode path (SA_PATH_AUTO or SA_PATH_FUSED_DECODE): when causal is
+ * 0 or 1, every sequence holds at most one query (cu_seqlens_q_host),
+ * head_dim is 128,
  * page_size is a power of two of at least 8, block_size / page_size <= 8,
  * block_size <= 64 or a multiple of 64, qhead <= 4 (f32 K/V) or <= 16 (bf16),
  * num_pages * hkv * page_size < 2^31 and tq * hq * 4 < 2^31, steps 2 and 3

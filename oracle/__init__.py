@@ -127,6 +127,17 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
+def causal_mode(causal) -> int:
+    """0 (none), 1 (right-aligned, the code's rule) or 2 (left-aligned, the
+    doc's reading for unknown KV lengths); booleans map to 0 / 1."""
+    if isinstance(causal, (bool, np.bool_)):
+        return int(causal)
+    c = int(causal)
+    if c not in (0, 1, 2):
+        raise ValueError(f"causal must be 0, 1 or 2, got {causal!r}")
+    return c
+
+
 def _check(code: int):
     if code != 0:
         raise OracleError(code)
@@ -275,7 +286,7 @@ def forward(q, k_pages, v_pages, index: dict, block_tables, cu_seqlens_q, used_k
                          _ptr(_c(index["edge_head_base"], np.int64)),
                          index["nbs"], index["msb"], _ptr(bt), index["max_pages"], _ptr(cu),
                          cu.size - 1, _ptr(used), hq, hkv, head_dim, block_size, page_size,
-                         softmax_scale, int(bool(causal)), _ptr(o), _ptr(m), _ptr(l))
+                         softmax_scale, causal_mode(causal), _ptr(o), _ptr(m), _ptr(l))
     _check(code)
     o = o[: E * qhead]
     if partial_dtype == "bf16":
@@ -342,7 +353,7 @@ def direct(q, k_pages, v_pages, selected, block_tables, cu_seqlens_q, used_kv_le
     lse = np.zeros(max(n, 1), np.float64)
     code = L.orc_direct(_ptr(qa), _ptr(k), _ptr(v), kb, num_pages, _ptr(sel), tq, hkv, topk,
                         _ptr(cu), cu.size - 1, _ptr(used), _ptr(bt), bt.shape[1], hq, head_dim,
-                        block_size, page_size, softmax_scale, int(bool(causal)), _ptr(rws),
+                        block_size, page_size, softmax_scale, causal_mode(causal), _ptr(rws),
                         0 if rws is None else n, _ptr(out), _ptr(lse))
     _check(code)
     if rws is None:

@@ -21,6 +21,9 @@
  *
  * Readings taken where the pages are silent (each also listed in the design
  * notes of the repository):
+ *   - causal = 1 is the right-aligned rule of the code; causal = 2 the
+ *     left-aligned variant (limit = the query's position in its chunk), an
+ *     opt-in for the doc's reading of unknown KV lengths.
  *   - msb = floor(max_pages / pages_per_block).
  *   - The index drops an entry when its id is -1 or when the block starts at
  *     or beyond the sequence's KV length (block_id * block_size >= lk_b); a
@@ -325,10 +328,15 @@ static int64_t gather_block_keys(int64_t b, int64_t blk, int64_t lk,
     return n;
 }
 
-/* Right-aligned causal limit of a query (forward.rs, kvouter_forward doc and
- * process_work_unit): keys at absolute position <= limit stay alive. */
-static int64_t causal_limit(int64_t lk, int64_t qo_len, int64_t q_local)
+/* Causal limit of a query: keys at absolute position <= limit stay alive.
+ * Mode 1, right-aligned (forward.rs, kvouter_forward doc and
+ * process_work_unit: the code's rule); mode 2, left-aligned (the doc's
+ * reading for unknown KV lengths: the query's own position in its chunk,
+ * an opt-in variant). */
+static int64_t causal_limit(int64_t lk, int64_t qo_len, int64_t q_local, int mode)
 {
+    if (mode == 2)
+        return q_local;
     if (lk >= qo_len)
         return lk - qo_len + q_local;
     return q_local;
@@ -379,7 +387,7 @@ int orc_forward(const float *q, const void *k_pages, const void *v_pages, int kv
             int64_t e1 = edge_head_base[h] + sel_offsets[h * (nbs + 1) + j + 1];
             for (int64_t e = e0; e < e1; ++e) {
                 int64_t q_idx = edges[2 * e];
-                int64_t limit = causal_limit(lk, qo_len, q_idx - cu_seqlens_q[b]);
+                int64_t limit = causal_limit(lk, qo_len, q_idx - cu_seqlens_q[b], causal);
                 for (int64_t qh = 0; qh < qhead; ++qh) {
                     int64_t hq_abs = h * qhead + qh;
                     const float *q_row = q + (q_idx * hq + hq_abs) * head_dim;
@@ -527,7 +535,7 @@ int orc_direct(const float *q, const void *k_pages, const void *v_pages, int kv_
         int64_t b = orc_batch_of(cu_seqlens_q, batch + 1, i);
         int64_t lk = seq_kv_len(used_kv_lens, b, msb, block_size);
         int64_t qo_len = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-        int64_t limit = causal_limit(lk, qo_len, i - cu_seqlens_q[b]);
+        int64_t limit = causal_limit(lk, qo_len, i - cu_seqlens_q[b], causal);
         const float *q_row = q + (i * hq + hq_abs) * head_dim;
 
         int64_t n = 0;

@@ -23,7 +23,8 @@ def uses_fused(w) -> bool:
     """Whether sa_attention (SA_PATH_AUTO) takes the fused decode path, which
     writes no partials."""
     return sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq, w.head_dim,
-                                       w.block_size, w.page_size, w.kv_dtype) == "fused_dec_kernel"
+                                       w.block_size, w.page_size, w.kv_dtype,
+                                       causal=w.causal) == "fused_dec_kernel"
 
 
 def auto_tol(w) -> float:

@@ -38,7 +38,8 @@ def dense_reference(q, k, v, block_tables, cu, used, hkv, head_dim, block_size, 
 
     Keys of sequence b are the positions p < lk_b whose page
     block_tables[b, p // page_size] is not -1; with `causal`, also p <= limit
-    (right-aligned).  Written with numpy matrix products, query-outer."""
+    (right-aligned; causal = 2: left-aligned, limit = the query's position in
+    its chunk).  Written with numpy matrix products, query-outer."""
     q = np.asarray(q, np.float64)
     kf = oracle_free_f64(k)
     vf = oracle_free_f64(v)
@@ -58,7 +59,7 @@ def dense_reference(q, k, v, block_tables, cu, used, hkv, head_dim, block_size, 
         qo = int(cu[b + 1] - cu[b])
         for t in range(qo):
             i = int(cu[b]) + t
-            limit = (lk - qo + t) if lk >= qo else t
+            limit = t if causal == 2 else ((lk - qo + t) if lk >= qo else t)
             alive = np.ones(pos.size, bool) if not causal else pos <= limit
             for h in range(hkv):
                 K = kf[pages, h, rows, :][alive]
@@ -225,9 +226,33 @@ def pin_dense_fixtures(L):
 
 def pin_dense_random(L, seeds=range(40)):
     for s in seeds:
-        for causal in (False, True):
+        for causal in (False, True, 2):
             c = random_case(s, bf16=(s % 3 == 0), pass_used=(s % 4 != 1))
             _vs_dense(c, causal, L, f"random seed={s} causal={causal}")
+
+
+def pin_causal_modes(L, seeds=range(12)):
+    """Left- and right-aligned limits coincide when every sequence's KV length
+    equals its query count (lk - qo + t = t), and differ otherwise; the
+    left-aligned first query of a chunk sees the block holding position 0
+    only through that one key."""
+    for s in seeds:
+        c = random_case(s, allow_empty_seq=False)
+        rng = np.random.default_rng(100 + s)
+        lens = rng.integers(1, c["msb"] * c["bs"] + 1, size=len(c["cu"]) - 1)
+        c["used"] = lens.astype(np.int32)                  # lk_b = qo_b
+        c["cu"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        tq = int(c["cu"][-1])
+        c["q"] = rng.standard_normal((tq, c["hq"], c["d"])).astype(np.float32)
+        c["sel"] = full_selection(tq, c["hkv"], c["msb"])
+        o1, l1, _, _, _, _ = _run_sparse(c, 1, L)
+        o2, l2, _, _, _, _ = _run_sparse(c, 2, L)
+        _close(o1, o2, 0.0, f"seed {s}: modes agree when lk == qo")
+        _close(l1, l2, 0.0, f"seed {s}: lse")
+    c = fixture_f1()
+    o1, _, _, _, _, _ = _run_sparse(c, 1, L)
+    o2, _, _, _, _, _ = _run_sparse(c, 2, L)
+    assert not np.allclose(o1, o2), "left-aligned equals right-aligned on a chunk with lk > qo"
 
 
 def pin_invariance(L, seeds=range(12)):
@@ -533,4 +558,4 @@ def pin_bf16_partials(L, seeds=range(8)):
 
 ALL_PINS = [pin_types, pin_dense_fixtures, pin_dense_random, pin_invariance, pin_single_block,
             pin_equal_keys, pin_partials, pin_index_bruteforce, pin_errors, pin_round_bf16,
-            pin_bf16_partials]
+            pin_bf16_partials, pin_causal_modes]

@@ -140,3 +140,26 @@ def test_fused_decode_path_refusals():
                       d.head_dim, d.block_size, d.page_size, d.softmax_scale, d.causal,
                       path=sa.PATH_FUSED_DECODE)
     assert e.value.kind == "UNSUPPORTED"
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_attention_graph_replay(dt):
+    """sa_attention captured into a CUDA graph (index, fused forward +
+    combine) and replayed after the inputs' contents change: the same out and
+    lse as eager calls on the new contents."""
+    w = decode_case(dt, 64, 16, 4 if dt == "f32" else 8, seed=44)
+    t = _gpu.device_workload(w)
+    g = sa.AttentionGraph(t["q"], t["k"], t["v"], t["selected"], w.cu_seqlens_q, t["cu"],
+                          t["used"], t["bt"], w.hq, w.hkv, w.head_dim, w.block_size,
+                          w.page_size, w.softmax_scale, w.causal)
+    rng = np.random.default_rng(3)
+    for it in range(3):
+        t["q"].copy_(torch.from_numpy(rng.standard_normal(tuple(t["q"].shape)).astype(np.float32)))
+        sel = w.selected.copy()
+        rng.shuffle(sel, axis=2)                       # the same blocks at other ranks
+        t["selected"].copy_(torch.from_numpy(sel))
+        out, lse = g.replay()
+        torch.cuda.synchronize()
+        assert sa.sa_get_status(g.index) == 0
+        ref_out, ref_lse, _, _ = _gpu.run_attention(w, t)
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)

@@ -239,3 +239,12 @@ def test_attention_kernel_choice(lib):
     assert name(one, 1000, 8, 32, 128, 48, 24, "f32") != "fused_dec_kernel"
     # head_dim 128 only
     assert name(one, 1000, 8, 32, 64, 64, 16, "f32") == "forward_cc_kernel"
+    # left-aligned causal (causal = 2) leaves the fused path; other modes are refused
+    assert name(one, *geo, "f32", causal=1) == "fused_dec_kernel"
+    assert name(one, *geo, "f32", causal=2) == "forward_dec_kernel"
+    assert name(one, *geo, "f32", sa.PATH_FUSED_DECODE, causal=2) is None
+    assert lib.sa_attention_kernel_name(4, 4, one.ctypes.data, 1000, 32, 8, 128, 64, 16, 0, 3,
+                                        0) is None
+    with pytest.raises(ValueError):
+        sa._causal(3)
+    assert [sa._causal(c) for c in (False, True, 0, 1, 2)] == [0, 1, 0, 1, 2]

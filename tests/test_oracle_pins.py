@@ -63,6 +63,8 @@ MUTATIONS = [
     ("bf16 rounding truncates", "double y = ldexp(rint(ldexp(x, -step)), step);",
      "double y = ldexp(trunc(ldexp(x, -step)), step);"),
     ("bf16 grid one bit too fine", "int step = k - 8;", "int step = k - 9;"),
+    ("left-aligned limit taken right-aligned", "    if (mode == 2)\n        return q_local;",
+     "    if (mode == 2)\n        return lk - qo_len + q_local;"),
     ("bf16 subnormal grid too coarse", "if (step < -133)\n        step = -133;",
      "if (step < -126)\n        step = -126;"),
 ]

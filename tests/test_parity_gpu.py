@@ -303,3 +303,47 @@ def test_tensor_core_bf16_q_copy_matches_f32_gather(name):
                                        split_edges=3, out=q_alias, path=sa.PATH_TENSOR_CORE)
     torch.cuda.synchronize()
     assert torch.equal(out3, out) and torch.equal(lse3, lse)
+
+
+LEFT_PATHS = {"auto": sa.PATH_AUTO, "cuda_core": sa.PATH_CUDA_CORE,
+              "cuda_core_general": sa.PATH_CUDA_CORE_GENERAL,
+              "tensor_core": sa.PATH_TENSOR_CORE}
+
+
+@pytest.mark.parametrize("path", list(LEFT_PATHS), ids=list(LEFT_PATHS))
+@pytest.mark.parametrize("name", ["gqa_decode", "chunked_prefill", "chunked_prefill_bf16",
+                                  "skewed", "long_decode"])
+def test_left_aligned_causal(name, path):
+    """causal = 2 (left-aligned: key p live for the t-th query of its chunk
+    iff p <= t) on every kernel; decode batches leave the fused path (a lone
+    query then sees key 0 at most)."""
+    w = inputs.small(name, seed=12)
+    w.causal = 2
+    p = LEFT_PATHS[path]
+    kernel = sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq, w.head_dim,
+                                         w.block_size, w.page_size, w.kv_dtype, path=p, causal=2)
+    if kernel is None:
+        pytest.skip("no kernel of this path for the shape")
+    assert kernel != "fused_dec_kernel"
+    tol = _gpu.TOL_TC if kernel == "forward_tc_kernel" or path == "tensor_core" else _gpu.TOL_F32
+    _check_against_oracle(w, _gpu.device_workload(w), 3, p, tol)
+
+
+@pytest.mark.parametrize("name", ["chunked_prefill", "skewed"])
+def test_attention_graph_replay_unfused(name):
+    """The unfused path (index, Q rounding pass, tensor-core forward,
+    combine) captured into a CUDA graph: replays after the queries change
+    equal eager calls."""
+    w = inputs.small(name, seed=13)
+    t = _gpu.device_workload(w)
+    g = sa.AttentionGraph(t["q"], t["k"], t["v"], t["selected"], w.cu_seqlens_q, t["cu"],
+                          t["used"], t["bt"], w.hq, w.hkv, w.head_dim, w.block_size,
+                          w.page_size, w.softmax_scale, w.causal, split_edges=3)
+    rng = np.random.default_rng(4)
+    for _ in range(2):
+        t["q"].copy_(torch.from_numpy(rng.standard_normal(tuple(t["q"].shape)).astype(np.float32)))
+        out, lse = g.replay()
+        torch.cuda.synchronize()
+        assert sa.sa_get_status(g.index) == 0
+        ref_out, ref_lse, _, _ = _gpu.run_attention(w, t, split_edges=3)
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
