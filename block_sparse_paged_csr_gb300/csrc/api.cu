@@ -314,6 +314,9 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
+  if (kernel == FwdKernel::kTensor && idx->workspace != nullptr && idx->workspace_bytes >= 256)
+    a.unit_counter = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(idx->workspace) +
+                                                 sa::workspace_layout(1, 1, 1, 0, 1).unit_ctr);
   if (kernel == FwdKernel::kTensor && q16_scratch != nullptr) {
     const int64_t n = idx->tq * static_cast<int64_t>(hq) * head_dim;
     err = sa::launch_q_to_bf16(q, static_cast<uint16_t*>(q16_scratch), n, s);

@@ -312,14 +312,27 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
   const int qhead = a.qhead;
   const int ps = a.page_size;
   int64_t* status = a.totals + 3;
-  uint32_t U = 0;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+  for (uint32_t U = 0;; ++U) {
     const int sl = static_cast<int>(U % kRing);
     unsigned char* slot = smem + P.ring + sl * P.slot_bytes;
     const bool got = U < static_cast<uint32_t>(kRing) ||
                      mbar_wait_bounded(B.slot_empty + sl, ((U / kRing) - 1) & 1u);
     if (!__all_sync(kAll, got)) {
       if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    // The next unit: claimed from the forward's counter (whichever CTA is
+    // free takes the next unit in index order, so heavy units of a skewed
+    // selection do not pile up on a few CTAs), or round-robin without one.
+    int64_t u = 0;
+    if (lane == 0)
+      u = a.unit_counter ? static_cast<int64_t>(atomicAdd(a.unit_counter, 1u))
+                         : blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
+    u = __shfl_sync(kAll, u, 0);
+    if (u >= n_units) {
+      // end of work: a unit with rows < 0 tells the other roles to stop
+      if (lane == 0) reinterpret_cast<UnitInfo*>(slot)->rows = -1;
+      mbar_arrive(B.slot_full + sl);
       return;
     }
     int h, j;
@@ -396,16 +409,15 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
 
 template <int BS, bool kBf16>
 __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
-                          const TcBars& B, const int32_t* unit_base, int64_t n_units, int lw,
-                          int lane) {
+                          const TcBars& B, int lw, int lane) {
   constexpr int KVB = TcCfg<BS>::KVB;
   constexpr int kNX = TcCfg<BS>::NX;
   using L = SlotLayout<BS>;
   const int lt = lw * 32 + lane;
   const int qhead = a.qhead;
   int64_t* status = a.totals + 3;
-  uint32_t U = 0, T = 0;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+  uint32_t T = 0;
+  for (uint32_t U = 0;; ++U) {
     const int kvb = static_cast<int>(U % KVB);
     unsigned char* ks = smem + P.kv + kvb * P.kv_bytes;
     unsigned char* vs = ks + static_cast<size_t>(BS) * kD * 2;
@@ -423,6 +435,13 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
     }
     // ---- the unit, as the scheduler resolved it ------------------------------
     const UnitInfo si = *reinterpret_cast<const UnitInfo*>(slot);
+    if (si.rows < 0) {
+      // end of work: passed on to the MMA and softmax roles through the unit
+      // buffer (freed above)
+      if (lt == 0) info->rows = -1;
+      mbar_arrive(B.kv_full + kvb);
+      return;
+    }
     const int rows = si.rows;
     const int h = si.h;
     const int64_t e0 = si.e0;
@@ -582,12 +601,12 @@ __device__ bool tc_issue_o(unsigned char* smem, const TcPlan& P, const TcBars& B
 
 template <int BS>
 __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
-                       const TcBars& B, uint32_t tmem, int64_t n_units) {
+                       const TcBars& B, uint32_t tmem) {
   constexpr int KVB = TcCfg<BS>::KVB;
   constexpr int kNX = TcCfg<BS>::NX;
   int64_t* status = a.totals + 3;
-  uint32_t U = 0, T = 0;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+  uint32_t T = 0;
+  for (uint32_t U = 0;; ++U) {
     const int kvb = static_cast<int>(U % KVB);
     if (!mbar_wait_bounded(B.kv_full + kvb, (U / KVB) & 1u)) {
       report(status, SA_ERR_DEVICE_TIMEOUT);
@@ -595,6 +614,7 @@ __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& 
     }
     const UnitInfo* info = reinterpret_cast<const UnitInfo*>(smem + P.info) + kvb;
     const int rows = info->rows;
+    if (rows < 0) return;                        // end of work
     const uint32_t k_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes);
     tc_fence_after();
     const int tiles = (rows + kM - 1) / kM;
@@ -681,8 +701,8 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 // parity g, and with them TMEM buffers S[g], O[g].
 template <int BS>
 __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsigned char* smem,
-                           const TcPlan& P, const TcBars& B, uint32_t tmem, int64_t n_units,
-                           int warp, int lane) {
+                           const TcPlan& P, const TcBars& B, uint32_t tmem, int warp,
+                           int lane) {
   const uint32_t g = static_cast<uint32_t>((warp - 1 - kLoaders) >> 2);
   constexpr int KVB = TcCfg<BS>::KVB;
   int64_t* status = a.totals + 3;
@@ -807,8 +827,8 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
     return true;
   };
 
-  uint32_t U = 0, T = 0;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++U) {
+  uint32_t T = 0;
+  for (uint32_t U = 0;; ++U) {
     const int kvb = static_cast<int>(U % KVB);
     const bool gk = mbar_wait_bounded(B.kv_full + kvb, (U / KVB) & 1u);
     if (!__all_sync(0xffffffffu, gk)) {
@@ -816,6 +836,7 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
       return;
     }
     const UnitInfo info = reinterpret_cast<const UnitInfo*>(smem + P.info)[kvb];
+    if (info.rows < 0) return;                          // end of work
     const int32_t* kpos = reinterpret_cast<const int32_t*>(smem + P.kpos) + kvb * BS;
     uint32_t vmask[BS / 32];
 #pragma unroll
@@ -1020,16 +1041,16 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
 
   if (warp == 0) {
     if (lane == 0) {
-      tc_mma<BS>(a, smem, P, B, tmem, n_units);
+      tc_mma<BS>(a, smem, P, B, tmem);
       // Every MMA issued has completed before TMEM is released.
       mma_commit(B.done);
       if (!mbar_wait_bounded(B.done, 0)) report(a.totals + 3, SA_ERR_DEVICE_TIMEOUT);
     }
     __syncwarp();
   } else if (warp <= kLoaders) {
-    tc_loader<BS, kBf16>(a, smem, P, B, unit_base, n_units, warp - 1, lane);
+    tc_loader<BS, kBf16>(a, smem, P, B, warp - 1, lane);
   } else if (warp < kSchedWarp) {
-    tc_softmax<BS>(a, &omap, smem, P, B, tmem, n_units, warp, lane);
+    tc_softmax<BS>(a, &omap, smem, P, B, tmem, warp, lane);
     // box stores issued by this thread have landed before the CTA leaves
     bulk_wait_all();
   } else {
@@ -1071,6 +1092,11 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       args.o_tma = 1;
+  }
+  // The work counter starts at zero for every launch.
+  if (args.unit_counter != nullptr) {
+    const cudaError_t e = cudaMemsetAsync(args.unit_counter, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
   }
   // One CTA per SM: it holds all 512 TMEM columns.
   int64_t grid = device_sm_count();

@@ -535,6 +535,7 @@ WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
   const size_t nseg = static_cast<size_t>(hkv) * batch;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   L.barrier = 0;
+  L.unit_ctr = 64;
   L.seg_done = 256;
   L.item_cnt = up(L.seg_done + 4 * nseg);
   L.seg_tot = up(L.item_cnt + 4 * static_cast<size_t>(hkv) * static_cast<size_t>(tq));

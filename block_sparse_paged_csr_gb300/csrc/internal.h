@@ -17,6 +17,8 @@ constexpr int kChunkEntries = 4096;
 // Layout of the index workspace (bytes from its start).
 struct WorkspaceLayout {
   size_t barrier;       // uint32[2]: grid barrier counter and generation
+  size_t unit_ctr;      // uint32: units claimed by a tensor-core forward (within the
+                        // barrier's 256-byte block, outside the index build's use)
   size_t seg_done;      // uint32[hkv*batch]: chunks of the segment that finished phase 1
   size_t item_cnt;      // uint32[tq*hkv]: finished pieces per (query, kv head), fused decode
   size_t seg_tot;       // int32[hkv*batch][3]: edges, non-empty bins, work splits
@@ -74,6 +76,8 @@ struct ForwardArgs {
   int o_bf16;
   int o_tma;                // set by a launcher: o rows may go out by tensor-map stores
   const uint16_t* q16;      // nullable: Q rounded to bf16, same layout (tensor-core kernel)
+  uint32_t* unit_counter;   // nullable: the tensor-core kernel's work counter (in the
+                            // index workspace; cleared by its launcher)
   float* m_partial;
   float* l_partial;
 };
