@@ -146,18 +146,28 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_digest(path: str) -> str:
+    """sha256 (16 hex digits) of a CUDA source's code: comments, trailing
+    blanks and empty lines removed, so that a comment edit does not detach a
+    profile from the code it was taken on."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    code = "\n".join(ln for ln in lines if ln)
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def ncu_traffic(kernel_file: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel (else None)."""
+    on the kernel's current code (else None)."""
     src = os.path.join(ROOT, "block_sparse_paged_csr_gb300", "csrc", kernel_file)
     prof = os.path.join(ROOT, "profiles", f"{kernel_file.split('.')[0]}_{workload}.md")
     if not (os.path.exists(src) and os.path.exists(prof)):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     text = open(prof).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256 ([0-9a-f]+)\)",
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(code sha256 ([0-9a-f]+)\)",
                   text)
-    if not m or m.group(2) != digest:
+    if not m or m.group(2) != code_digest(src):
         return None
     return float(m.group(1))
 

@@ -3,38 +3,41 @@
 // alice-llm's sparse_attention) for work units with many gathered rows
 // (chunked prefill, skewed selections).
 //
-// A persistent CTA per SM takes (kv head, block) units round-robin, so the
-// SMs working at the same time cover neighbouring blocks of one (kv head,
-// sequence) and share its Q rows in L2.  A unit's rows (edge x GQA lane) go
-// through 128-row tiles.  Warp roles, coupled by mbarriers:
-//   warp 23    scheduler: runs up to four units ahead of the loaders and
+// A persistent CTA per SM claims (kv head, block) units in index order from a
+// per-launch counter (whichever CTA is free takes the next unit, so the heavy
+// units of a skewed selection spread out), so the SMs working at the same
+// time cover neighbouring blocks of one (kv head, sequence) and share its Q
+// rows in L2.  A unit's rows (edge x GQA lane) go through 128-row tiles.
+// Warp roles, coupled by mbarriers:
+//   warp 23    scheduler: claims units up to four ahead of the loaders and
 //              resolves each unit's index entries (slot, edge range,
 //              sequence, KV length), its keys' positions and page offsets
 //              through the block table, and the Q row sources of its first
 //              tile into a ring of unit slots, so that the loaders start
-//              every unit with its global addresses at hand;
+//              every unit with its global addresses at hand; an end-of-work
+//              unit stops the other roles;
 //   warps 1-14 loaders: per unit, the block's K and V rows (through the
 //              block table, f32 or bf16) converted to bf16 once, both as
 //              [keys x 128] rows with the 128-byte swizzle: K-major for S,
 //              MN-major for O (two unit buffers, so the next unit loads
-//              while this one computes); per tile, the rows' Q (f32 -> bf16,
-//              same layout) (two or three tile buffers, so the gathers'
-//              latency stays off the path);
+//              while this one computes); per tile, the rows' Q in the same
+//              layout, from a bf16 copy of Q when the caller gives scratch
+//              for one, else f32 rows converted (two or three tile buffers,
+//              so the gathers' latency stays off the path);
 //   warp 0     one thread issues S = Q K^T (M=128, N=block, K=128) into TMEM
 //              and, once the softmax has turned S into P, O = P V (M=128,
 //              N=128, K=block; P from TMEM); tcgen05.commit signals the
 //              mbarriers;
 //   warps 15-22 softmax and epilogue, two warpgroups taking alternate tiles
 //              (and the matching S / O buffer), thread t <-> row t of the
-//              tile (TMEM lane t): S back
-//              with tcgen05.ld, masks (block length, absent pages,
-//              right-aligned causal limit), m, p = exp(s - m), l, and P as
-//              bf16 pairs back into S's TMEM columns (tcgen05.st), where the
-//              second MMA takes it as its A operand; the tile buffer thus
-//              holds Q only and frees as soon as S is done; then the
-//              previous tile's O back from
-//              TMEM and its unnormalised partial row (staged through shared
-//              memory for whole-line stores), m and l to memory.
+//              tile (TMEM lane t): S back with tcgen05.ld, masks (block
+//              length, absent pages, causal limit), m, p = 2^(s q - m), l,
+//              and P as bf16 pairs back into S's TMEM columns (tcgen05.st),
+//              where the second MMA takes it as its A operand; the tile
+//              buffer thus holds Q only and frees as soon as S is done; then
+//              the previous tile's O back from TMEM and its unnormalised
+//              partial row through a swizzled staging tile, as TMA box
+//              stores for full 32-row warps, and m and l to memory.
 // S and O are double-buffered in TMEM (512 columns), so S of tile t + 1 and
 // the epilogue of tile t - 1 overlap the softmax of tile t.  Operands are
 // rounded to bf16 (tolerance class of the tensor-core path); S, O and the

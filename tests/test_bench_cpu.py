@@ -76,3 +76,14 @@ def test_profiles_match_kernel_sources(kernel, workload):
                                        f"{kernel.split('.')[0]}_{workload}.md"))
     t = bench.ncu_traffic(kernel, workload)
     assert t is not None and t > 0, f"profile of {kernel} on {workload} is stale: re-capture it"
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) {  /* note */\n  return x + 1;  // one\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// another header\n\nint f(int x) {\n  return x + 1;\n}\n/* tail\n   note */\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.code_digest(str(a)) == bench.code_digest(str(b))
+    assert bench.code_digest(str(a)) != bench.code_digest(str(c))
