@@ -244,7 +244,11 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * twice the batch) to the pipelined CUDA-core kernel (f32 K/V) or to the
  * warp-level MMA kernel (bf16 K/V), and the others to the tcgen05 kernel
  * where supported (operands rounded to bf16; use SA_PATH_CUDA_CORE for f32
- * arithmetic throughout).  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * arithmetic throughout).  The tcgen05 kernel claims work units from a
+ * counter in the first 256 bytes of idx->workspace (cleared on the stream
+ * before each launch) when idx->workspace is set and idx->workspace_bytes is
+ * at least 256, else it takes them round-robin; so one index serves one
+ * forward at a time.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
  * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
  */
 sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
