@@ -38,7 +38,7 @@ class SaIndex(ctypes.Structure):
         ("msb", ctypes.c_int32),
         ("nbs", ctypes.c_int64),
         ("split_edges", ctypes.c_int32),
-        ("reserved_", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("sel_slots", ctypes.c_void_p),
         ("sel_offsets", ctypes.c_void_p),
         ("num_sel", ctypes.c_void_p),

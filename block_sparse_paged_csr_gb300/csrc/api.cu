@@ -219,6 +219,7 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   idx->msb = static_cast<int32_t>(msb);
   idx->nbs = nbs;
   idx->split_edges = split_edges;
+  idx->flags = 0;
 
   sa::IndexArgs a{};
   a.selected = selected;
@@ -240,6 +241,23 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
 }
 
 namespace {
+
+// The scratch an index's forward takes its counters from: the library's
+// fixed array for an index built by sa_build_index_no_alloc, else the
+// caller's workspace.  Returns false when there is none (NULL workspace).
+bool index_scratch(const sa_index* idx, unsigned char** ws, size_t* bytes) {
+  void* p = nullptr;
+  size_t n = 0;
+  if (idx->flags & SA_INDEX_STATIC_SCRATCH) {
+    if (sa::static_index_scratch(&p, &n) != SA_OK) p = nullptr;
+  } else {
+    p = idx->workspace;
+    n = idx->workspace_bytes;
+  }
+  *ws = static_cast<unsigned char*>(p);
+  *bytes = p != nullptr ? n : 0;
+  return p != nullptr;
+}
 
 // Step 2.  `q16_scratch` (nullable): room for tq * hq * head_dim bf16 values,
 // 16-byte aligned, not overlapping q, that the tensor-core kernel may fill
@@ -314,9 +332,11 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   if (a.msb <= 0) return SA_OK;  // no block is addressable: every entry was dropped
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (kernel == FwdKernel::kTensor && idx->workspace != nullptr && idx->workspace_bytes >= 256)
-    a.unit_counter = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(idx->workspace) +
-                                                 sa::workspace_layout(1, 1, 1, 0, 1).unit_ctr);
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (kernel == FwdKernel::kTensor && index_scratch(idx, &ws, &ws_bytes) && ws_bytes >= 256)
+    a.unit_counter =
+        reinterpret_cast<uint32_t*>(ws + sa::workspace_layout(1, 1, 1, 0, 1).unit_ctr);
   if (kernel == FwdKernel::kTensor && q16_scratch != nullptr) {
     const int64_t n = idx->tq * static_cast<int64_t>(hq) * head_dim;
     err = sa::launch_q_to_bf16(q, static_cast<uint16_t*>(q16_scratch), n, s);
@@ -491,7 +511,14 @@ sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void*
                          lse, stream);
   }
   if (!q || !k_pages || !v_pages || !block_tables || !cu_seqlens_q || !selected || !o_partial ||
-      !m_partial || !l_partial || !out || !idx->inv || !idx->workspace || !idx->totals)
+      !m_partial || !l_partial || !out || !idx->inv || !idx->totals)
+    return SA_ERR_INVALID_ARGUMENT;
+  // The per-(query, kv head) piece counters live in the index's scratch,
+  // cleared by the build that made the index.
+  unsigned char* ws = nullptr;
+  size_t ws_bytes = 0;
+  const sa::WorkspaceLayout lay = sa::workspace_layout(hkv, batch, tq, 0, 1);
+  if (!index_scratch(idx, &ws, &ws_bytes) || ws_bytes < lay.seg_tot)
     return SA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o_partial) ||
       !aligned16(out))
@@ -544,8 +571,7 @@ sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void*
   a.pieces = (a.topk + ep - 1) / ep;
   a.scale = softmax_scale;
   a.status = idx->totals + 3;
-  a.item_cnt = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(idx->workspace) +
-                                           sa::workspace_layout(hkv, batch, tq, 0, 1).item_cnt);
+  a.item_cnt = reinterpret_cast<uint32_t*>(ws + lay.item_cnt);
   a.part_o = o_partial;
   a.part_bf16 = partial_dtype == SA_DTYPE_BF16 ? 1 : 0;
   a.part_m = m_partial;

@@ -156,6 +156,10 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
 int device_sm_count();
 
+// The fixed scratch array of sa_build_index_no_alloc on the current device
+// (no_alloc.cu): its device address and size.
+sa_status static_index_scratch(void** ptr, size_t* bytes);
+
 // cuTensorMapEncodeTiled from the driver (NULL if unavailable); looked up once.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

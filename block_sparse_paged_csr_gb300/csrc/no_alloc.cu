@@ -8,9 +8,14 @@
 // or a host runtime that has no allocator to hand.  They still own the index
 // arrays and the selection inputs; only the scratch moves into the library.
 //
-// The scratch holds the index kernel's segment ticket and per-segment status
-// words (see index.cu).  Every GPU that loads this library keeps its own copy
-// of the array until the process exits.
+// The scratch holds what the index build keeps outside the index arrays
+// (workspace_layout in index.cu): the grid barrier, the segment tickets, one
+// counter per (query, kv head) for the fused decode kernel, the segment
+// totals and prefixes, and the histograms of multi-chunk segments.  An index
+// built here carries SA_INDEX_STATIC_SCRATCH, and the forward entry points
+// then take their counters from this array too (index_scratch in api.cu).
+// Every GPU that loads this library keeps its own copy of the array until the
+// process exits.
 #include <cstdint>
 #include <mutex>
 
@@ -19,9 +24,10 @@
 
 namespace {
 
-// 288 KiB: 40 bytes per (kv head, sequence) segment, plus, for sequences
-// with more than 4096 (query, rank) entries per kv head, msb 4-byte counters
-// per 4096 entries (see workspace_layout in index.cu).
+// 288 KiB.  Per (kv head, sequence) segment 40 bytes (ticket 4, totals 12,
+// prefixes 24), per (query, kv head) 4 bytes, per 4096-entry chunk of a
+// multi-chunk segment msb 4-byte bins, plus the barrier block and roundings
+// to 256 bytes (workspace_layout in index.cu; the formula is in sa.h).
 constexpr size_t kStaticScratchBytes = 288 * 1024;
 
 static __device__ __align__(256) unsigned char g_index_scratch[kStaticScratchBytes];
@@ -49,6 +55,16 @@ sa_status scratch_for_current_device(void** out) {
 }
 
 }  // namespace
+
+namespace sa {
+
+sa_status static_index_scratch(void** ptr, size_t* bytes) {
+  const sa_status st = scratch_for_current_device(ptr);
+  if (st == SA_OK) *bytes = kStaticScratchBytes;
+  return st;
+}
+
+}  // namespace sa
 
 extern "C" sa_status sa_build_index_no_alloc(const int32_t* selected, int64_t tq, int32_t hkv,
                                              int32_t topk, const int64_t* cu_seqlens_q_host,
@@ -86,6 +102,7 @@ extern "C" sa_status sa_build_index_no_alloc(const int32_t* selected, int64_t tq
     *idx = local;
     idx->workspace = keep_ws;
     idx->workspace_bytes = keep_bytes;
+    idx->flags = SA_INDEX_STATIC_SCRATCH;
   }
   return st;
 }

@@ -105,7 +105,7 @@ typedef struct sa_index {
   int32_t msb;
   int64_t nbs;
   int32_t split_edges;       /* largest number of edges in one work split (0 = no cut) */
-  int32_t reserved_;
+  int32_t flags;             /* SA_INDEX_* bits, written by the build entry points  */
 
   /* device arrays, caller-allocated */
   int32_t *sel_slots;        /* [hkv, nbs]   compact slot j -> raw slot; -1 for j >= num_sel[h] */
@@ -122,6 +122,11 @@ typedef struct sa_index {
   void *workspace;           /* scratch, sa_index_sizes.workspace_bytes, 256-byte aligned       */
   size_t workspace_bytes;
 } sa_index;
+
+/* sa_index.flags bit: the index was built by sa_build_index_no_alloc, so its
+ * scratch (the counters that the forward entry points read after the build)
+ * lives in the library's fixed array on that device, not in idx->workspace. */
+#define SA_INDEX_STATIC_SCRATCH 1
 
 /* Element counts of each sa_index array and the workspace size in bytes. */
 typedef struct sa_index_sizes {
@@ -184,20 +189,38 @@ sa_status sa_build_index(const int32_t *selected, int64_t tq, int32_t hkv, int32
 /*
  * sa_build_index without a workspace: the pages have no counterpart; this is
  * a library convenience.  Same arguments, checks and results as
- * sa_build_index, except that idx->workspace / workspace_bytes are ignored
- * (left unchanged) and the build's scratch comes from a 288 KiB array
- * compiled into the library, one copy per GPU that loads it, held until the
- * process exits.
+ * sa_build_index, except that the build's scratch comes from a 288 KiB array
+ * compiled into the library (one copy per GPU that loads it, held until the
+ * process exits) instead of idx->workspace, which may be NULL and is left
+ * unchanged.  The call sets SA_INDEX_STATIC_SCRATCH in idx->flags;
+ * sa_build_index clears it.
  *
  * For callers that cannot allocate device memory when they call: servers
  * whose device memory is reserved up front, code running under a memory cap,
  * or host runtimes without a device allocator.  The call itself allocates
  * nothing (no cudaMalloc, cudaFree or allocating library routine).
  *
- *   - Returns SA_ERR_UNSUPPORTED when the problem needs more scratch than
- *     the array holds: 16 bytes per (kv head, sequence) segment (so at most
- *     about 18,000 segments), plus, for sequences with more than 4096
- *     (query, rank) entries per kv head, msb 4-byte counters per 4096 entries.
+ *   - Capacity.  With S = hkv * batch segments, M = the 4096-entry chunks of
+ *     the sequences holding more than 4096 (query, rank) entries per kv head
+ *     (sum over those sequences of ceil(qo_len * topk / 4096)), and up(x) =
+ *     x rounded up to a multiple of 256, the scratch is
+ *         a = up(256 + 4 S)            segment tickets
+ *         b = up(a + 4 hkv tq)         counters per (query, kv head)
+ *         c = up(b + 12 S)             segment totals
+ *         d = up(c + 24 (S + 1))       segment prefixes
+ *         total = up(d + 4 hkv M msb)  histograms of multi-chunk segments
+ *     bytes; a problem with total > 294912 (288 KiB) returns
+ *     SA_ERR_UNSUPPORTED before any device work.  With one query per
+ *     sequence and topk <= 4096 (M = 0) that is about 40 bytes per segment
+ *     plus 4 bytes per (query, kv head): up to 6,687 sequences at hkv = 1
+ *     or 835 at hkv = 8.  The decode shapes (64 or 128 sequences of
+ *     one query, hkv 8) fit; prefill-sized problems (thousands of queries
+ *     per sequence) do not and need sa_build_index.
+ *   - The forward entry points take the index's counters (the fused decode
+ *     kernel's piece counters, which this build clears, and the tensor-core
+ *     kernel's work counter) from the same array: run them on the index
+ *     before the next sa_build_index_no_alloc call on that device, which
+ *     reuses the array.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture on the device.
@@ -245,10 +268,11 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * warp-level MMA kernel (bf16 K/V), and the others to the tcgen05 kernel
  * where supported (operands rounded to bf16; use SA_PATH_CUDA_CORE for f32
  * arithmetic throughout).  The tcgen05 kernel claims work units from a
- * counter in the first 256 bytes of idx->workspace (cleared on the stream
- * before each launch) when idx->workspace is set and idx->workspace_bytes is
- * at least 256, else it takes them round-robin; so one index serves one
- * forward at a time.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * counter in the first 256 bytes of the index's scratch (cleared on the
+ * stream before each launch): idx->workspace when it is set and
+ * idx->workspace_bytes is at least 256, the library's array for an index
+ * with SA_INDEX_STATIC_SCRATCH; with neither it takes units round-robin.  So
+ * one index serves one forward at a time.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
  * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
  */
 sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
@@ -386,7 +410,12 @@ sa_status sa_combine_ex(const sa_index *idx, sa_dtype partial_dtype, const void 
  * SMs are cut into pieces to fill the SMs; split_edges > 0 cuts every pair
  * into pieces of split_edges ranks (at most 64).  Pieces of one pair are
  * merged through rows of the partial buffers, whose content afterwards is
- * unspecified.  out and lse equal those of the unfused path up to rounding.
+ * unspecified, and counted in one 4-byte counter per (query, kv head) that
+ * the index build clears in its scratch (idx->workspace, or the library's
+ * array for an index with SA_INDEX_STATIC_SCRATCH) and the kernel leaves at
+ * zero: sa_forward_combine on this path returns SA_ERR_INVALID_ARGUMENT when
+ * that scratch is missing or smaller than the build's layout.  out and lse
+ * equal those of the unfused path up to rounding.
  */
 sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,
                        int64_t num_pages, sa_dtype kv_dtype, const int32_t *selected,

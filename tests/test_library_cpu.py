@@ -248,3 +248,26 @@ def test_attention_kernel_choice(lib):
     with pytest.raises(ValueError):
         sa._causal(3)
     assert [sa._causal(c) for c in (False, True, 0, 1, 2)] == [0, 1, 0, 1, 2]
+
+
+def test_no_alloc_capacity_host_check(lib):
+    """sa_build_index_no_alloc refuses, before any device work, exactly the
+    problems whose scratch (the formula in sa.h) exceeds its 288 KiB array:
+    835 one-query sequences at hkv = 8 pass the size check, 836 do not."""
+    from block_sparse_paged_csr_gb300 import _native
+
+    def call(batch):
+        cu = np.arange(batch + 1, dtype=np.int64)
+        idx = _native.SaIndex()
+        return lib.sa_build_index_no_alloc(None, batch, 8, 4, cu.ctypes.data_as(ctypes.c_void_p),
+                                           None, batch, None, 40, 64, 16, 0, ctypes.byref(idx),
+                                           None)
+
+    assert _native.STATUS_NAMES[call(836)] == "UNSUPPORTED"
+    assert _native.STATUS_NAMES[call(835)] != "UNSUPPORTED"
+    # a prefill-sized problem (4 x 2048 queries, topk 32, hkv 8, msb 256) does not fit
+    cu = np.array([0, 2048, 4096, 6144, 8192], np.int64)
+    idx = _native.SaIndex()
+    rc = lib.sa_build_index_no_alloc(None, 8192, 8, 32, cu.ctypes.data_as(ctypes.c_void_p), None,
+                                     4, None, 512, 128, 64, 0, ctypes.byref(idx), None)
+    assert _native.STATUS_NAMES[rc] == "UNSUPPORTED"
