@@ -1,7 +1,7 @@
 """Benchmark of KV-outer block-sparse paged attention (index + forward +
 combine) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all]
                     [--impl reference]
 
 One step is one pass of the whole path (sa_attention: CSR index build,
@@ -9,20 +9,33 @@ KV-outer forward, log-sum-exp combine) over one batch of the workload, with
 every input resident in HBM.  Between timed steps L2 is flushed by writing a
 512 MiB buffer (outside the step's CUDA events).  Prints one JSON line.
 
---impl reference times the oracle (plain f64 C, one host thread) on a bounded
-sample of the same workload; it is a reported CPU baseline.
+With --workload all (the default) the headline is the long-context decode
+workload (128 sequences of one query over 64-131 K keys, a 69 GB bf16 K/V
+pool: the largest single-GPU configuration) and the line carries one
+sub-record per other serving workload (GQA decode, chunked prefill with f32
+and with bf16 K/V, skewed selection), each measured the same way with its
+own steps, roofline, end-to-end rate and CPU baseline.
 
-Under torchrun (N > 1) every rank runs its own replica of the workload (its own
-seed) on its own GPU: the path has no exchange step, so there is no data
-collective; a barrier and a max-reduction of the elapsed time bracket the run.
+The CPU baseline is the oracle (plain f64 C) as it stands, run on the host's
+cores by one thread per core over a bounded sample of the workload: shards of
+(sequence, kv head, query rows), each an independent sub-problem because a
+q-head reads only its own kv head.  --impl reference times the same oracle,
+every step one such sample.
+
+Under torchrun (N > 1) every rank runs its own replica of the workloads (its
+own seed) on its own GPU: the path has no exchange step, so there is no data
+collective; a barrier and a max-reduction of the elapsed time bracket each
+timed region.
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import math
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -42,6 +55,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 SPLIT_EDGES = {"tiny": 0, "gqa_decode": 0, "chunked_prefill": 16, "chunked_prefill_bf16": 16,
                "skewed": 16, "long_decode": 0}
+HEADLINE = "long_decode"
+SUB_WORKLOADS = ("gqa_decode", "chunked_prefill", "chunked_prefill_bf16", "skewed")
 
 
 def parse_args():
@@ -49,11 +64,15 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gqa_decode")
+    ap.add_argument("--workload", default="all",
+                    help="'all' (headline long_decode + the other serving workloads as "
+                         "sub-records) or one workload name")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=4.0,
+                    help="wall seconds of oracle work per phase of each CPU baseline")
     ap.add_argument("--partials", default="f32", choices=["f32", "bf16"],
                     help="o partial storage: f32 (the pages' layout) or the opt-in bf16")
     return ap.parse_args()
@@ -269,7 +288,9 @@ def job_throughput(queries_per_step, steps, world, elapsed_s):
     return world * queries_per_step * steps / elapsed_s
 
 
-def run_ours(args, rank, world, local_rank):
+def measure_workload(name, args, rank, world, local_rank):
+    """Time K steps of sa_attention on one workload (plus per-stage and
+    end-to-end timings).  Returns (record or None on ranks > 0, workload)."""
     import torch
 
     import block_sparse_paged_csr_gb300 as sa
@@ -277,8 +298,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = make_workload(args.workload, args.seed + rank)
-    split = SPLIT_EDGES.get(args.workload.replace("_ncu", ""), 0)
+    w = make_workload(name, args.seed + rank)
+    split = SPLIT_EDGES.get(name.replace("_ncu", ""), 0)
     fwd_kernel = sa.sa_attention_kernel_name(w.cu_seqlens_q, w.num_pages, w.hkv, w.hq,
                                              w.head_dim, w.block_size, w.page_size, w.kv_dtype,
                                              causal=w.causal)
@@ -304,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     status = sa.sa_get_status(index)
     if status != 0:
-        raise RuntimeError(f"device status {sa.sa_status_string(status)}")
+        raise RuntimeError(f"{name}: device status {sa.sa_status_string(status)}")
     for _ in range(max(args.warmup, 3)):
         step(index, partials, out, lse)
     torch.cuda.synchronize(dev)
@@ -315,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps of the fused path ----------------------------
+    # ---- timed region: K steps of the whole path -----------------------------
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
@@ -336,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
     total_ms = float(sum(step_ms))
     status = sa.sa_get_status(index)
     if status != 0:
-        raise RuntimeError(f"device status {sa.sa_status_string(status)}")
+        raise RuntimeError(f"{name}: device status {sa.sa_status_string(status)}")
 
     # ---- per-stage durations (same launches, events between the stages) -----
     # On the fused decode path steps 2 and 3 are one kernel (sa_forward_combine).
@@ -408,14 +429,18 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": w.tq * n_e2e / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e}
+        del h_q, h_out, h_lse, d_q, d_sel, d_bt, d_cu, d_used
 
     # ---- aggregate over ranks -----------------------------------------------
     elapsed_s, e2e_total = aggregate_ranks(total_ms / 1e3, e2e["value"] if e2e else None, world,
                                            dev)
     if e2e is not None:
         e2e["value"] = e2e_total
+    del q, k, v, sel, cu, used, bt, flush, out, lse, index, partials, o_p, m_p, l_p
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     if rank != 0:
-        return None
+        return None, w
 
     peak, peak_kind = measured_peak()
     ms_per_step = elapsed_s * 1e3 / args.steps
@@ -423,16 +448,16 @@ def run_ours(args, rank, world, local_rank):
     step_gbs = acct["step"] / (ms_per_step / 1e3) / 1e9
     kv_gbs = acct["kv"] / (ms_per_step / 1e3) / 1e9
     fwd_file = fwd_kernel.replace("_kernel", ".cu")
-    traffic = ncu_traffic(fwd_file, args.workload.replace("_ncu", "") +
+    traffic = ncu_traffic(fwd_file, name.replace("_ncu", "") +
                           ("_bf16p" if args.partials == "bf16" and not fused else ""))
     value = job_throughput(w.tq, args.steps, world, elapsed_s)
     dtype = "f32" if w.kv_dtype == "f32" else "bf16-kv/f32"
-    return {
+    rec = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "config": {
-            "workload": args.workload, "batch": w.batch, "tq": w.tq, "hq": w.hq, "hkv": w.hkv,
+            "workload": name, "batch": w.batch, "tq": w.tq, "hq": w.hq, "hkv": w.hkv,
             "head_dim": w.head_dim, "page_size": w.page_size, "block_size": w.block_size,
             "topk": w.topk, "max_pages": w.max_pages, "num_pages": w.num_pages,
             "kv_dtype": w.kv_dtype, "causal": w.causal, "split_edges": split,
@@ -464,104 +489,241 @@ def run_ours(args, rank, world, local_rank):
                         * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
-        "cpu_baseline": (cpu_baseline(w, args)
-                         if world == 1 and not args.no_cpu_baseline else None),
     }
+    return rec, w
+
+
+def run_ours(args, rank, world, local_rank):
+    names = ([HEADLINE, *SUB_WORKLOADS] if args.workload == "all" else [args.workload])
+    records, workloads = [], []
+    for name in names:
+        rec, w = measure_workload(name, args, rank, world, local_rank)
+        records.append(rec)
+        workloads.append(w)
+    if rank != 0:
+        return None
+    # the oracle on the host cores, after every GPU timing (rank 0, N = 1 only)
+    for rec, w in zip(records, workloads):
+        rec["cpu_baseline"] = (cpu_baseline(w, args)
+                               if world == 1 and not args.no_cpu_baseline else None)
+    head = records[0]
+    if len(records) > 1:
+        head["sub_records"] = records[1:]
+    return head
 
 
 # --------------------------------------------------------------------------- oracle timing
 
 
-def sub_workload(w, seqs):
-    """The same workload restricted to the given sequences (a bounded sample)."""
-    import dataclasses
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
-    seqs = np.asarray(seqs)
+
+def oracle_threads() -> int:
+    return max(1, min(os.cpu_count() or 1, 64))
+
+
+def shard_costs(w, row_block):
+    """The workload cut into independent shards (sequence b, kv head h, query
+    rows [a, a + n) of b), each with an estimate of its oracle work: the
+    multiply-adds of its kept entries' blocks (two per key and dimension, per
+    GPU lane)."""
     cu = w.cu_seqlens_q
-    rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in seqs]).astype(np.int64)
-    sub = dataclasses.replace(w, batch=len(seqs), qo_lens=w.qo_lens[seqs],
-                              used_kv_lens=w.used_kv_lens[seqs], selected=w.selected[rows],
-                              block_tables=w.block_tables[seqs])
-    q = w.q_host()[rows]
-    return sub, q
+    shards = []
+    for b in range(w.batch):
+        qo = int(cu[b + 1] - cu[b])
+        if qo == 0:
+            continue
+        lk = max(int(w.used_kv_lens[b]), 0) if w.pass_used else w.msb * w.block_size
+        step = qo if qo <= row_block else row_block
+        for h in range(w.hkv):
+            for a in range(0, qo, step):
+                n = min(step, qo - a)
+                sel = w.selected[int(cu[b]) + a:int(cu[b]) + a + n, h]
+                kept = int(np.sum((sel >= 0) & (sel.astype(np.int64) * w.block_size < lk)))
+                cost = kept * w.qhead * w.block_size * w.head_dim * 2
+                shards.append((b, h, a, n, cost))
+    return shards
 
 
-def time_oracle(w, seqs, repeat_until_s):
-    """Oracle queries/s on the sample: index + partials + combine."""
+def make_shard(w, b, h, a, n):
+    """Oracle inputs of one shard: queries [a, a + n) of sequence b against kv
+    head h alone (q-heads h * qhead .. h * qhead + qhead - 1), with only the
+    pages its kept blocks touch.  Under the right-aligned causal rule a
+    sub-range of a sequence's queries is posed as a sequence of n queries whose
+    KV length is lk - qo + a + n: each query's limit lk - qo + t is unchanged,
+    so its output is too (blocks past the limit would be fully masked)."""
+    import inputs
+
+    cu = w.cu_seqlens_q
+    qo = int(cu[b + 1] - cu[b])
+    lk = max(int(w.used_kv_lens[b]), 0) if w.pass_used else w.msb * w.block_size
+    if n < qo and w.causal:
+        assert lk >= qo, "sub-ranges need lk >= qo under the causal rule"
+        lk_sub = lk - qo + a + n
+    else:
+        lk_sub = lk
+    rows = np.arange(int(cu[b]) + a, int(cu[b]) + a + n)
+    sel = np.ascontiguousarray(w.selected[rows][:, h:h + 1, :])
+    d, qh = w.head_dim, w.qhead
+    qidx = ((rows[:, None] * w.hq + h * qh) * d + np.arange(qh * d)[None, :]).astype(np.uint64)
+    q = inputs.counter_normal_at(w.seed, inputs.STREAM_Q, qidx).reshape(n, qh, d)
+    blocks = np.unique(sel[(sel >= 0) & (sel.astype(np.int64) * w.block_size < lk_sub)])
+    bt_row = w.block_tables[b].astype(np.int64)
+    cols = (blocks[:, None].astype(np.int64) * w.ppb + np.arange(w.ppb)[None, :]).ravel()
+    pages = np.unique(bt_row[cols][bt_row[cols] >= 0])
+    pos = np.searchsorted(pages, bt_row)
+    hit = (bt_row >= 0) & (pos < pages.size)
+    hit[hit] = pages[pos[hit]] == bt_row[hit]
+    bt = np.where(hit, pos, -1).astype(np.int32)[None, :]
+    pe, hs = w.page_elems, w.page_size * d
+
+    def pool(stream):
+        if pages.size == 0:
+            vals = np.zeros((1, 1, w.page_size, d), np.float32)
+        else:
+            idx = (pages[:, None] * pe + h * hs + np.arange(hs)[None, :]).astype(np.uint64)
+            vals = inputs.counter_normal_at(w.seed, stream, idx).reshape(pages.size, 1,
+                                                                         w.page_size, d)
+        return inputs.bf16_bits(vals) if w.kv_dtype == "bf16" else vals
+
+    return {"q": q, "k": pool(inputs.STREAM_K), "v": pool(inputs.STREAM_V), "sel": sel, "bt": bt,
+            "cu": np.array([0, n], np.int64),
+            "used": np.array([lk_sub], np.int32) if (w.pass_used or lk_sub != lk) else None,
+            "hq": qh, "queries": n / w.hkv}
+
+
+def pick_shards(w, budget_macs, row_block, rng_seed=0):
+    """Shards in a seeded random order until their estimated work reaches
+    budget_macs (at least one)."""
+    shards = shard_costs(w, row_block)
+    order = np.random.default_rng(rng_seed).permutation(len(shards))
+    picked, acc = [], 0
+    for j in order:
+        picked.append(shards[j])
+        acc += shards[j][4]
+        if acc >= budget_macs:
+            break
+    return picked
+
+
+def assign_lpt(shards, threads):
+    """Longest-first assignment of shards to threads (by estimated cost)."""
+    bins = [[] for _ in range(threads)]
+    load = [0] * threads
+    for s in sorted(shards, key=lambda s: -s[4]):
+        t = int(np.argmin(load))
+        bins[t].append(s)
+        load[t] += s[4]
+    return [b for b in bins if b]
+
+
+def run_oracle_phases(w, groups, pool, phases=("index", "partials_combine", "direct")):
+    """Run the oracle over prepared shard groups (one group per thread), one
+    phase at a time; returns wall seconds per phase."""
     import oracle
 
-    sub, q = sub_workload(w, seqs)
-    k, v, bt, _ = sub.compact_pool()
-    n = 0
-    t_total = 0.0
-    while True:
+    state = [[None] * len(g) for g in groups]
+
+    def index_part(t):
+        for j, s in enumerate(groups[t]):
+            state[t][j] = oracle.build_index(s["sel"], s["cu"], s["used"], w.max_pages,
+                                             w.block_size, w.page_size, 0)
+
+    def fwd_part(t):
+        for j, s in enumerate(groups[t]):
+            idx = state[t][j]
+            o, m, l = oracle.forward(s["q"], s["k"], s["v"], idx, s["bt"], s["cu"], s["used"],
+                                     s["hq"], w.head_dim, w.softmax_scale, w.causal)
+            oracle.combine(idx, s["hq"], w.head_dim, o, m, l)
+
+    def direct_part(t):
+        for s in groups[t]:
+            oracle.direct(s["q"], s["k"], s["v"], s["sel"], s["bt"], s["cu"], s["used"],
+                          s["hq"], w.head_dim, w.block_size, w.page_size, w.softmax_scale,
+                          w.causal)
+
+    fns = {"index": index_part, "partials_combine": fwd_part, "direct": direct_part}
+    walls = {}
+    for ph in phases:
         t0 = time.perf_counter()
-        oracle.attention(q, k, v, sub.selected, bt, sub.cu_seqlens_q, sub.used, sub.hq,
-                         sub.head_dim, sub.block_size, sub.page_size, sub.softmax_scale,
-                         sub.causal)
-        t_total += time.perf_counter() - t0
-        n += 1
-        if t_total >= repeat_until_s:
-            break
-    return sub.tq * n / t_total, n, sub.tq
+        list(pool.map(fns[ph], range(len(groups))))
+        walls[ph] = time.perf_counter() - t0
+    return walls
 
 
-def sample_sequences(w, target_queries):
-    """Leading sequences of the workload holding about target_queries queries."""
-    acc, seqs = 0, []
-    for b in range(w.batch):
-        seqs.append(b)
-        acc += int(w.qo_lens[b])
-        if acc >= target_queries:
-            break
-    return seqs
+CALIB_NS_PER_MAC = 2.5       # single-thread oracle speed, for sizing the samples only
+
+
+def oracle_sample(w, wall_s, threads, seed=0):
+    """Prepared shard groups whose partials phase should take about wall_s
+    seconds on `threads` host threads."""
+    import oracle
+
+    oracle.build()
+    row_block = 32 if w.tq > 2 * w.batch else 1
+    budget = wall_s * threads / (CALIB_NS_PER_MAC * 1e-9)
+    shards = pick_shards(w, budget, row_block, seed)
+    groups_meta = assign_lpt(shards, threads)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        groups = list(ex.map(lambda g: [make_shard(w, b, h, a, n) for (b, h, a, n, _) in g],
+                             groups_meta))
+    queries = sum(s["queries"] for g in groups for s in g)
+    desc = (f"{len(shards)} shard(s) (sequence, kv head, query rows) in a seeded random order, "
+            f"{queries:g} query-equivalents (query x kv head / hkv)")
+    return groups, queries, desc
 
 
 def cpu_baseline(w, args):
-    import oracle
-
-    oracle.build()
-    target = {"gqa_decode": 16, "long_decode": 4, "tiny": 4}.get(args.workload, 64)
-    seqs = sample_sequences(w, target)
-    qps, n, nq = time_oracle(w, seqs, repeat_until_s=10.0)
-    return {"value": qps, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {len(seqs)} sequence(s) ({nq} queries) of the workload, "
-                      f"full index + partials + combine in f64, repeated {n}x (~10 s)"}
+    """The oracle timed on the host cores: index, partials + combine, and the
+    query-outer direct attention, each as queries/s over the same sample;
+    `value` is the path (index + partials + combine)."""
+    threads = oracle_threads()
+    groups, queries, desc = oracle_sample(w, args.cpu_seconds, threads)
+    with cf.ThreadPoolExecutor(max_workers=len(groups)) as ex:
+        walls = run_oracle_phases(w, groups, ex)
+    path_s = walls["index"] + walls["partials_combine"]
+    return {"value": queries / path_s, "unit": UNIT, "cores": len(groups), "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "rates": {ph: queries / s for ph, s in walls.items()},
+            "sample": f"{desc}; one host thread per core, f64"}
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step runs the index and the
+    partials + combine over one bounded sample of the workload on the host
+    cores (rank 0 only)."""
     if rank != 0:
         return None
-    import inputs
-    import oracle
-
-    oracle.build()
-    w = make_workload(args.workload, args.seed)
-    target = {"gqa_decode": 1, "long_decode": 1, "tiny": 4}.get(args.workload, 2)
-    seqs = sample_sequences(w, target)
-    sub, q = sub_workload(w, seqs)
-    k, v, bt, _ = sub.compact_pool()
-
-    def one():
-        oracle.attention(q, k, v, sub.selected, bt, sub.cu_seqlens_q, sub.used, sub.hq,
-                         sub.head_dim, sub.block_size, sub.page_size, sub.softmax_scale,
-                         sub.causal)
-
-    for _ in range(args.warmup):
-        one()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        one()
-    el = time.perf_counter() - t0
-    value = sub.tq * args.steps / el
+    workload = HEADLINE if args.workload == "all" else args.workload
+    w = make_workload(workload, args.seed)
+    threads = oracle_threads()
+    per_step = getattr(args, "ref_step_seconds", 1.0)
+    groups, queries, desc = oracle_sample(w, per_step, threads)
+    phases = ("index", "partials_combine")
+    with cf.ThreadPoolExecutor(max_workers=len(groups)) as ex:
+        for _ in range(args.warmup):
+            run_oracle_phases(w, groups, ex, phases)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run_oracle_phases(w, groups, ex, phases)
+        el = time.perf_counter() - t0
+    value = queries * args.steps / el
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_queries_per_step": sub.tq},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"first {len(seqs)} sequence(s) ({sub.tq} queries) "
-                                       f"per step"},
+            "config": {"workload": workload, "sample_queries_per_step": queries},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(groups), "kind": "oracle",
+                             "cpu_model": cpu_model(),
+                             "sample": f"{desc} per step; one host thread per core, f64"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -60,7 +60,12 @@ def _splitmix64(x: np.ndarray) -> np.ndarray:
 
 def counter_normal(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """float32 values of elements [start, start+count) of tensor `stream`."""
-    idx = np.arange(start, start + count, dtype=np.uint64)
+    return counter_normal_at(seed, stream, np.arange(start, start + count, dtype=np.uint64))
+
+
+def counter_normal_at(seed: int, stream: int, idx: np.ndarray) -> np.ndarray:
+    """float32 values of the elements with flat indices `idx` of tensor `stream`."""
+    idx = np.asarray(idx, dtype=np.uint64)
     with np.errstate(over="ignore"):
         key = np.uint64(seed * 16 + stream)
         z = _splitmix64(idx + key * _MUL_KEY)

@@ -73,6 +73,25 @@ def row_error(got, ref):
     return float(np.max(np.max(np.abs(got - ref), axis=1) / den, initial=0.0))
 
 
+def elementwise_error(got, ref, floor=1e-6):
+    """The pages' own metric (gpu.rs, the test comparing the shader with the
+    CPU forward): max over elements of |got - ref| / max(|ref|, floor)."""
+    got = np.asarray(got, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), floor)))
+
+
+#: (test, quantity, row-normalised error, the pages' element-wise error) of
+#: the parity tests, printed at the end of the session (conftest.py).
+REPORT = []
+
+
+def report(test, quantity, got, ref):
+    REPORT.append((test, quantity, row_error(got, ref), elementwise_error(got, ref)))
+
+
 def compare_lse(got, ref, tol):
     got = np.asarray(got, np.float64).ravel()
     ref = np.asarray(ref, np.float64).ravel()

@@ -39,3 +39,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The measured errors of the parity tests: the row-normalised metric the
+    tests assert, next to the pages' element-wise metric (relative with a 1e-6
+    floor)."""
+    try:
+        import _gpu
+    except Exception:
+        return
+    if not _gpu.REPORT:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity errors: row-normalised | element-wise (rel, 1e-6 floor)")
+    for test, qty, row, elem in _gpu.REPORT:
+        tr.write_line(f"{test:60s} {qty:10s} {row:10.3e} {elem:10.3e}")

@@ -87,3 +87,42 @@ def test_code_digest_ignores_comments_only(tmp_path):
     c.write_text("int f(int x) {\n  return x + 2;\n}\n")
     assert bench.code_digest(str(a)) == bench.code_digest(str(b))
     assert bench.code_digest(str(a)) != bench.code_digest(str(c))
+
+
+@pytest.mark.parametrize("name", ["gqa_decode", "chunked_prefill", "skewed",
+                                  "chunked_prefill_bf16", "long_decode"])
+def test_cpu_baseline_shards_are_independent_sub_problems(orc, name):
+    """The CPU baseline's shards (sequence, kv head, query rows) reproduce the
+    whole problem's outputs for their rows: the oracle on a shard equals the
+    oracle on the full workload, so the baseline times real work of the
+    workload (and a sub-range of a causal sequence keeps each query's
+    limit)."""
+    w = inputs.small(name, seed=2)
+    full_out, full_lse, _, _ = orc.attention(w.q_host(), w.k_host(), w.v_host(), w.selected,
+                                             w.block_tables, w.cu_seqlens_q, w.used, w.hq,
+                                             w.head_dim, w.block_size, w.page_size,
+                                             w.softmax_scale, w.causal)
+    row_block = 16 if w.tq > 2 * w.batch else 1
+    shards = bench.shard_costs(w, row_block)
+    assert sum(s[3] for s in shards) == w.tq * w.hkv
+    cu = w.cu_seqlens_q
+    for b, h, a, n, _ in shards[:: max(1, len(shards) // 12)]:
+        s = bench.make_shard(w, b, h, a, n)
+        out, lse, _, _ = orc.attention(s["q"], s["k"], s["v"], s["sel"], s["bt"], s["cu"],
+                                       s["used"], s["hq"], w.head_dim, w.block_size, w.page_size,
+                                       w.softmax_scale, w.causal)
+        rows = np.arange(int(cu[b]) + a, int(cu[b]) + a + n)
+        ref = full_out[rows][:, h * w.qhead:(h + 1) * w.qhead]
+        assert np.allclose(out, ref, rtol=1e-12, atol=1e-12), (b, h, a, n)
+        ref_lse = full_lse[rows][:, h * w.qhead:(h + 1) * w.qhead]
+        assert np.array_equal(np.isfinite(lse), np.isfinite(ref_lse))
+        fin = np.isfinite(ref_lse)
+        assert np.allclose(lse[fin], ref_lse[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_cpu_baseline_runs_threads(orc):
+    w = inputs.small("skewed", seed=1)
+    args = type("A", (), {"cpu_seconds": 0.2})()
+    r = bench.cpu_baseline(w, args)
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] >= 1
+    assert set(r["rates"]) == {"index", "partials_combine", "direct"}

@@ -42,7 +42,10 @@ def test_small_workload_parity(name, split):
     if not _gpu.uses_fused(w):      # the fused decode path keeps its partials on chip
         _gpu.compare_partials(o[:rows].cpu().numpy(), m[:rows].cpu().numpy(),
                               l[:rows].cpu().numpy(), ro, rm, rl, tol)
+        _gpu.report(f"small {name} split {split}", "o_partial", o[:rows].cpu().numpy(), ro)
+        _gpu.report(f"small {name} split {split}", "l_partial", l[:rows].cpu().numpy(), rl)
     assert _gpu.row_error(out.cpu().numpy(), ref_out) <= tol
+    _gpu.report(f"small {name} split {split}", "out", out.cpu().numpy(), ref_out)
     _gpu.compare_lse(lse.cpu().numpy(), ref_lse, tol)
 
 
@@ -178,7 +181,7 @@ def test_full_size_workload(name):
     outputs on sampled rows against the oracle's query-outer attention."""
     w = inputs.FULL[name](0)
     t = _gpu.device_workload(w, fill_on_device=True)
-    out, lse, idx, _ = _gpu.run_attention(w, t, split_edges=SPLIT[name])
+    out, lse, idx, parts = _gpu.run_attention(w, t, split_edges=SPLIT[name])
     ref_idx = oracle.build_index(w.selected, w.cu_seqlens_q, w.used, w.max_pages, w.block_size,
                                  w.page_size, SPLIT[name])
     _gpu.compare_index(idx.to_host(), ref_idx)
@@ -194,9 +197,56 @@ def test_full_size_workload(name):
     got = out[rows[:, 0], rows[:, 1]].cpu().numpy()
     tol = _gpu.auto_tol(w)
     assert _gpu.row_error(got, ref) <= tol
+    _gpu.report(f"full {name} sampled rows", "out", got, ref)
     _gpu.compare_lse(lse[rows[:, 0], rows[:, 1]].cpu().numpy(), ref_lse, tol)
+    if not _gpu.uses_fused(w):
+        _check_hot_units(w, idx.to_host(), parts, 8 if name == "skewed" else 1, tol, name)
     del t
     torch.cuda.empty_cache()
+
+
+def _check_hot_units(w, ih, parts, n_units, tol, name):
+    """Every partial row of the n_units units with the most edges, against the
+    oracle's query-outer attention over that unit's block alone (a one-block
+    selection: out = o / l, lse = m + log l of the partial)."""
+    o_p, m_p, l_p = parts
+    q = w.q_host()
+    cand = []
+    for h in range(w.hkv):
+        offs = ih["sel_offsets"][h]
+        cnt = np.diff(offs[: int(ih["num_sel"][h]) + 1])
+        for j in np.argsort(-cnt, kind="stable")[:n_units]:
+            cand.append((int(cnt[j]), h, int(j)))
+    cand.sort(key=lambda c: -c[0])
+    for cnt, h, j in cand[:n_units]:
+        raw = int(ih["sel_slots"][h, j])
+        b, blk = divmod(raw, w.msb)
+        e0 = int(ih["edge_head_base"][h]) + int(ih["sel_offsets"][h, j])
+        edges = ih["edges"][e0:e0 + cnt]
+        pages = w.block_tables[b, blk * w.ppb:(blk + 1) * w.ppb]
+        live = pages >= 0
+        k, v = w.k_host(pages[live]), w.v_host(pages[live])
+        bt = np.full_like(w.block_tables, -1)
+        bt[b, blk * w.ppb:(blk + 1) * w.ppb][live] = np.arange(int(live.sum()), dtype=np.int32)
+        sel1 = np.full((w.tq, w.hkv, 1), -1, np.int32)
+        sel1[edges[:, 0], h, 0] = blk
+        rows = np.array([(int(i), h * w.qhead + qh) for i, _ in edges for qh in range(w.qhead)])
+        ref, ref_lse = oracle.direct(q, k, v, sel1, bt, w.cu_seqlens_q, w.used, w.hq,
+                                     w.head_dim, w.block_size, w.page_size, w.softmax_scale,
+                                     w.causal, rows=rows)
+        prow = (np.arange(e0, e0 + cnt)[:, None] * w.qhead + np.arange(w.qhead)[None, :]).ravel()
+        sel_rows = torch.from_numpy(prow).to(o_p.device)
+        o = o_p[sel_rows].float().cpu().numpy().astype(np.float64)
+        m = m_p[sel_rows].cpu().numpy().astype(np.float64)
+        l = l_p[sel_rows].cpu().numpy().astype(np.float64)
+        live_rows = l > 0
+        assert np.array_equal(live_rows, np.isfinite(ref_lse)), "empty partial rows differ"
+        got = np.zeros_like(o)
+        got[live_rows] = o[live_rows] / l[live_rows, None]
+        assert _gpu.row_error(got, ref) <= tol, f"unit ({h}, {raw}) with {cnt} edges"
+        _gpu.report(f"full {name} unit of {cnt} edges", "o/l", got, ref)
+        lse_got = np.where(live_rows, m + np.log(np.where(live_rows, l, 1.0)), -np.inf)
+        _gpu.compare_lse(lse_got, ref_lse, tol)
 
 
 # --------------------------------------------------------------------------- each kernel
