@@ -103,6 +103,15 @@ def make_workload(name: str, seed: int):
         w = inputs.long_decode(seed, batch=128, kv_min=8192, kv_max=12288)
         w.name = name
         return w
+    if name.endswith("_idx"):
+        # captures of the index kernel: the full workload's selection, lengths
+        # and tables (so the same index work), its block tables folded onto a
+        # pool of 8192 pages so that the capture holds little device memory
+        w = inputs.FULL[name[:-4]](seed)
+        w.block_tables = np.where(w.block_tables >= 0, w.block_tables % 8192, -1).astype(np.int32)
+        w.num_pages = 8192
+        w.name = name
+        return w
     return inputs.FULL[name](seed)
 
 
@@ -484,8 +493,9 @@ def measure_workload(name, args, rank, world, local_rank):
         "e2e": e2e,
         # library kernels per step: the index kernel, then the fused decode
         # kernel, or forward + combine (the tensor-core forward preceded by
-        # the pass that rounds Q to bf16 into its scratch)
-        "gpu_launches": (2 if fused else (4 if fwd_kernel == "forward_tc_kernel" else 3))
+        # the pass that rounds Q to bf16 into its scratch and by the one that
+        # sorts its units longest-first)
+        "gpu_launches": (2 if fused else (5 if fwd_kernel == "forward_tc_kernel" else 3))
                         * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,

@@ -26,14 +26,19 @@ import torch
 
 from . import _native
 from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_CUDA_CORE_GENERAL,
-                      PATH_FUSED_DECODE, PATH_TENSOR_CORE, STATUS_NAMES)
+                      PATH_FUSED_DECODE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_BF16, STATUS_NAMES)
 
 __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
            "sa_build_index_no_alloc", "sa_forward", "sa_forward_combine", "sa_forward_kernel_name",
            "sa_attention_kernel_name", "PATH_FUSED_DECODE",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
-           "PATH_CUDA_CORE_GENERAL", "AttentionGraph"]
+           "PATH_TENSOR_CORE_BF16",
+           "PATH_CUDA_CORE_GENERAL", "AttentionGraph", "sa_debug_stall", "sa_debug_cta_stats", "STALL_NONE",
+           "STALL_INDEX_BARRIER", "STALL_FUSED_COPIES"]
+
+#: sa_debug_stall sites (a test hook: see include/sa.h)
+STALL_NONE, STALL_INDEX_BARRIER, STALL_FUSED_COPIES = 0, 1, 2
 
 
 class SAError(RuntimeError):
@@ -480,3 +485,23 @@ def sa_get_status(index: Index, stream=None) -> int:
 def sa_clear_status(index: Index, stream=None) -> None:
     _check(_native.load().sa_clear_status(ctypes.byref(index.c), _stream(stream, index.device)),
            "sa_clear_status")
+
+
+def sa_debug_stall(site: int, spin_limit: int = 0) -> None:
+    """Test hook: make the bounded wait at ``site`` run out on every launch
+    from now on (STALL_INDEX_BARRIER, STALL_FUSED_COPIES), with ``spin_limit``
+    tries per wait (0 = the library default); STALL_NONE restores normal
+    operation."""
+    _check(_native.load().sa_debug_stall(int(site), int(spin_limit)), "sa_debug_stall")
+
+
+def sa_debug_cta_stats(stats=None) -> None:
+    """Test hook: with ``stats`` (a zeroed int64 CUDA tensor of 3 * n_ctas
+    elements) every later tensor-core forward adds each CTA's claimed rows
+    and units and writes its busy cycles there; None turns it off."""
+    if stats is None:
+        _check(_native.load().sa_debug_cta_stats(None, 0), "sa_debug_cta_stats")
+        return
+    _require(stats, torch.int64, "stats")
+    _check(_native.load().sa_debug_cta_stats(_ptr(stats), stats.numel() // 3),
+           "sa_debug_cta_stats")

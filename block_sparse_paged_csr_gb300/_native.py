@@ -16,13 +16,14 @@ STATUS_NAMES = {
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL, PATH_FUSED_DECODE = 0, 1, 2, 3, 4
+PATH_TENSOR_CORE_BF16 = 5
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",
            "sa_build_index_no_alloc", "sa_forward", "sa_forward_ex", "sa_forward_combine",
            "sa_forward_combine_ex", "sa_forward_kernel_name", "sa_attention_kernel_name",
            "sa_combine", "sa_combine_ex", "sa_attention", "sa_attention_ex", "sa_get_status",
-           "sa_clear_status")
+           "sa_clear_status", "sa_debug_stall", "sa_debug_cta_stats")
 
 
 class SaIndex(ctypes.Structure):
@@ -118,6 +119,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_get_status.restype = st
     lib.sa_clear_status.argtypes = [ctypes.POINTER(SaIndex), p]
     lib.sa_clear_status.restype = st
+    lib.sa_debug_stall.argtypes = [i32, ctypes.c_uint32]
+    lib.sa_debug_stall.restype = st
+    lib.sa_debug_cta_stats.argtypes = [p, i32]
+    lib.sa_debug_cta_stats.restype = st
     if path == LIB_PATH:
         _lib = lib
     return lib

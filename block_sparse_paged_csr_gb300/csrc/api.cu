@@ -1,6 +1,7 @@
 // C ABI of libsa (declared in include/sa.h): argument checks in the order of
 // kvouter_forward's "argument sanity" (forward.rs) and of the error enum
 // (types.rs), then kernel launches on the caller's stream.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -22,6 +23,26 @@ EncodeTiledFn encode_fn() {
     return reinterpret_cast<EncodeTiledFn>(p);
   }();
   return fn;
+}
+
+namespace {
+std::atomic<int> g_stall_site{kStallNone};
+std::atomic<uint32_t> g_spin_limit{0};
+}  // namespace
+
+namespace {
+std::atomic<int64_t*> g_cta_stats{nullptr};
+std::atomic<int32_t> g_cta_stats_len{0};
+}  // namespace
+
+void debug_cta_stats(int64_t** buf, int32_t* n_ctas) {
+  *n_ctas = g_cta_stats_len.load(std::memory_order_relaxed);
+  *buf = *n_ctas > 0 ? g_cta_stats.load(std::memory_order_relaxed) : nullptr;
+}
+
+void debug_stall_setting(int* site, uint32_t* spin_limit) {
+  *site = g_stall_site.load(std::memory_order_relaxed);
+  *spin_limit = g_spin_limit.load(std::memory_order_relaxed);
 }
 
 int device_sm_count() {
@@ -59,6 +80,7 @@ FwdKernel choose_forward(int64_t tq, int32_t batch, int32_t qhead, int32_t head_
   const bool cc_ok = sa::forward_cc_supported(head_dim, block_size, kv_bf16);
   switch (path) {
     case SA_PATH_TENSOR_CORE:
+    case SA_PATH_TENSOR_CORE_BF16:
       if (decode_like && mma_ok) return FwdKernel::kDecodeMma;
       return tc_ok ? FwdKernel::kTensor : FwdKernel::kNone;
     case SA_PATH_CUDA_CORE:
@@ -173,10 +195,10 @@ sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t ba
   out->inv = n;
   out->splits = 4 * n;
   out->totals = 4;
-  out->workspace_bytes =
-      sa::workspace_layout(hkv, batch, tq, sa::index_hist_slot_bound(tq, topk),
-                           static_cast<int32_t>(msb))
-          .total;
+  // the build's scratch, then the tensor-core forward's longest-first work list
+  const sa::LptRegion lpt =
+      sa::lpt_region(tq, hkv, topk, batch, static_cast<int32_t>(msb), nbs);
+  out->workspace_bytes = lpt.offset + lpt.bytes;
   return SA_OK;
 }
 
@@ -285,7 +307,7 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   if (path == SA_PATH_FUSED_DECODE) return SA_ERR_UNSUPPORTED;   // writes no partials
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
-      path != SA_PATH_TENSOR_CORE)
+      path != SA_PATH_TENSOR_CORE && path != SA_PATH_TENSOR_CORE_BF16)
     return SA_ERR_INVALID_ARGUMENT;
   const FwdKernel kernel = choose_forward(idx->tq, idx->batch, hq / hkv, head_dim, block_size,
                                           page_size, kv_bf16, path);
@@ -334,10 +356,20 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   cudaError_t err;
   unsigned char* ws = nullptr;
   size_t ws_bytes = 0;
-  if (kernel == FwdKernel::kTensor && index_scratch(idx, &ws, &ws_bytes) && ws_bytes >= 256)
+  if (kernel == FwdKernel::kTensor && index_scratch(idx, &ws, &ws_bytes) && ws_bytes >= 256) {
     a.unit_counter =
         reinterpret_cast<uint32_t*>(ws + sa::workspace_layout(1, 1, 1, 0, 1).unit_ctr);
-  if (kernel == FwdKernel::kTensor && q16_scratch != nullptr) {
+    const sa::LptRegion lpt =
+        sa::lpt_region(idx->tq, idx->hkv, idx->topk, idx->batch, idx->msb, idx->nbs);
+    if (ws_bytes >= lpt.offset + lpt.bytes) {
+      a.unit_order = reinterpret_cast<int32_t*>(ws + lpt.offset);
+      a.max_units = lpt.units;
+    }
+  }
+  if (kernel == FwdKernel::kTensor) sa::debug_cta_stats(&a.cta_stats, &a.cta_stats_len);
+  // f32 K/V stay f32 (tf32 operands) unless bf16 operands are asked for
+  a.tf32 = kernel == FwdKernel::kTensor && !kv_bf16 && path != SA_PATH_TENSOR_CORE_BF16;
+  if (kernel == FwdKernel::kTensor && !a.tf32 && q16_scratch != nullptr) {
     const int64_t n = idx->tq * static_cast<int64_t>(hq) * head_dim;
     err = sa::launch_q_to_bf16(q, static_cast<uint16_t*>(q16_scratch), n, s);
     if (err != cudaSuccess) return SA_ERR_CUDA;
@@ -626,7 +658,7 @@ sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pag
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
   }
   if (!fused && !sa::forward_cc_supported(head_dim, block_size, kv_bf16) &&
-      !(path == SA_PATH_TENSOR_CORE &&
+      !((path == SA_PATH_TENSOR_CORE || path == SA_PATH_TENSOR_CORE_BF16) &&
         sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv)))
     return SA_ERR_UNSUPPORTED;
   const sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q,
@@ -654,6 +686,20 @@ sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,
                          max_pages, hq, hkv, head_dim, block_size, page_size, softmax_scale,
                          causal, split_edges, idx, SA_DTYPE_F32, o_partial, m_partial, l_partial,
                          out, lse, path, stream);
+}
+
+sa_status sa_debug_stall(int32_t site, uint32_t spin_limit) {
+  if (site < sa::kStallNone || site > sa::kStallFusedCopies) return SA_ERR_INVALID_ARGUMENT;
+  sa::g_stall_site.store(site, std::memory_order_relaxed);
+  sa::g_spin_limit.store(spin_limit, std::memory_order_relaxed);
+  return SA_OK;
+}
+
+sa_status sa_debug_cta_stats(int64_t* stats, int32_t n_ctas) {
+  if (n_ctas < 0 || (n_ctas > 0 && stats == nullptr)) return SA_ERR_INVALID_ARGUMENT;
+  sa::g_cta_stats.store(n_ctas > 0 ? stats : nullptr, std::memory_order_relaxed);
+  sa::g_cta_stats_len.store(n_ctas, std::memory_order_relaxed);
+  return SA_OK;
 }
 
 sa_status sa_get_status(const sa_index* idx, void* stream) {

@@ -102,6 +102,43 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// D (TMEM) (+)= A (smem) x B (smem)^T, tf32 inputs (f32 in shared memory),
+// f32 accumulation.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM, row i in lane i, one tf32 per column) x B (smem)^T.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -177,6 +214,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn = fals
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor: tf32 x tf32 -> f32 (operand format 2), A K-major,
+// B K-major or (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int m, int n, bool b_mn = false) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (b_mn ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Byte offset of a 16-byte chunk of f32 elements inside a K-major,
+// 128B-swizzled tile of `rows` rows: element k (a multiple of 4) of row r,
+// 32 f32 per panel row.
+__device__ __forceinline__ uint32_t sw128_offset_f32(int rows, int r, int k) {
+  const int panel = k >> 5;
+  const int chunk = (k & 31) >> 2;
+  return static_cast<uint32_t>(panel * rows * 128 + r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
 // Byte offset of element pair/quad position inside a K-major, 128B-swizzled
 // tile of `rows` rows: element k of row r (bf16 elements, 64 per panel row).
 __device__ __forceinline__ uint32_t sw128_offset(int rows, int r, int k) {
@@ -202,12 +255,15 @@ constexpr int kLoadThreads = 32 * kLoaders;
 constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 10
 constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
 
-template <int BS> struct TcCfg {
-  static constexpr int KVB = 2;                   // unit buffers (K, V)
-  static constexpr int NX = BS == 128 ? 2 : 3;    // tile buffers (Q)
+// kTf32: operands kept in f32 (tcgen05 kind::tf32) instead of rounded to
+// bf16; every shared-memory tile is then twice as large.
+template <int BS, bool kTf32 = false> struct TcCfg {
+  static constexpr int E = kTf32 ? 4 : 2;         // bytes per operand element
+  static constexpr int KVB = kTf32 && BS == 128 ? 1 : 2;     // unit buffers (K, V)
+  static constexpr int NX = kTf32 ? 1 : (BS == 128 ? 2 : 3); // tile buffers (Q)
   // epilogue staging tiles per warp: two where shared memory allows (the
   // box store of one drains while the other fills)
-  static constexpr int SB = BS == 128 ? 1 : 2;
+  static constexpr int SB = !kTf32 && BS == 64 ? 2 : 1;
 };
 constexpr int kMaxNX = 3;
 constexpr int kRing = 4;                          // unit slots of the scheduler
@@ -248,15 +304,15 @@ __host__ __device__ constexpr size_t tc_up(size_t x, size_t a) { return (x + a -
 // Every region starts on a 128-byte boundary (the swizzled tiles on 1024):
 // float4 staging, int64 offsets and mbarriers all need their alignment
 // whatever the sizes of the regions before them.
-__host__ __device__ inline TcPlan tc_plan(int bs) {
-  const int kvb = bs == 128 ? TcCfg<128>::KVB : TcCfg<64>::KVB;
-  const int nx = bs == 128 ? TcCfg<128>::NX : TcCfg<64>::NX;
-  const int sb = bs == 128 ? TcCfg<128>::SB : TcCfg<64>::SB;
+template <int BS, bool kTf32>
+__host__ __device__ inline TcPlan tc_plan() {
+  using C = TcCfg<BS, kTf32>;
+  const int bs = BS, kvb = C::KVB, nx = C::NX, sb = C::SB;
   TcPlan p{};
-  p.kv_bytes = static_cast<size_t>(bs) * kD * 2 * 2;
+  p.kv_bytes = static_cast<size_t>(bs) * kD * C::E * 2;
   p.kv = 0;                                                             // 1024-aligned
-  p.x = p.kv + kvb * p.kv_bytes;                                        // [nx] tiles of 32 KB
-  p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * 2, 128);     // int32 [kvb][BS]
+  p.x = p.kv + kvb * p.kv_bytes;                                        // [nx] Q tiles
+  p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * C::E, 128);  // int32 [kvb][BS]
   p.info = tc_up(p.kpos + kvb * static_cast<size_t>(bs) * 4, 128);      // UnitInfo [kvb]
   p.slot_bytes = bs == 128 ? SlotLayout<128>::bytes : SlotLayout<64>::bytes;
   p.ring = tc_up(p.info + kvb * sizeof(UnitInfo), 128);                 // slots [kRing]
@@ -327,10 +383,17 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     // The next unit: claimed from the forward's counter (whichever CTA is
     // free takes the next unit in index order, so heavy units of a skewed
     // selection do not pile up on a few CTAs), or round-robin without one.
+    // With a longest-first list the counter walks that list instead.
     int64_t u = 0;
-    if (lane == 0)
-      u = a.unit_counter ? static_cast<int64_t>(atomicAdd(a.unit_counter, 1u))
-                         : blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
+    if (lane == 0) {
+      if (a.unit_counter != nullptr) {
+        const uint32_t k = atomicAdd(a.unit_counter, 1u);
+        u = (a.unit_order != nullptr && k < n_units) ? static_cast<int64_t>(a.unit_order[k])
+                                                     : static_cast<int64_t>(k);
+      } else {
+        u = blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
+      }
+    }
     u = __shfl_sync(kAll, u, 0);
     if (u >= n_units) {
       // end of work: a unit with rows < 0 tells the other roles to stop
@@ -393,6 +456,11 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
       }
       qsrc[r] = src;
     }
+    if (lane == 0 && a.cta_stats != nullptr && static_cast<int>(blockIdx.x) < a.cta_stats_len) {
+      unsigned long long* st = reinterpret_cast<unsigned long long*>(a.cta_stats) + 3 * blockIdx.x;
+      atomicAdd(st, static_cast<unsigned long long>(rows));
+      atomicAdd(st + 1, 1ull);
+    }
     if (lane == 0) {
       UnitInfo* info = reinterpret_cast<UnitInfo*>(slot);
       info->rows = rows;
@@ -410,11 +478,12 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
 
 // ------------------------------------------------------------------ loaders
 
-template <int BS, bool kBf16>
+template <int BS, bool kBf16, bool kTf32>
 __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
                           const TcBars& B, int lw, int lane) {
-  constexpr int KVB = TcCfg<BS>::KVB;
-  constexpr int kNX = TcCfg<BS>::NX;
+  constexpr int KVB = TcCfg<BS, kTf32>::KVB;
+  constexpr int kNX = TcCfg<BS, kTf32>::NX;
+  constexpr int E = TcCfg<BS, kTf32>::E;
   using L = SlotLayout<BS>;
   const int lt = lw * 32 + lane;
   const int qhead = a.qhead;
@@ -423,7 +492,7 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
   for (uint32_t U = 0;; ++U) {
     const int kvb = static_cast<int>(U % KVB);
     unsigned char* ks = smem + P.kv + kvb * P.kv_bytes;
-    unsigned char* vs = ks + static_cast<size_t>(BS) * kD * 2;
+    unsigned char* vs = ks + static_cast<size_t>(BS) * kD * E;
     int32_t* kpos = reinterpret_cast<int32_t*>(smem + P.kpos) + kvb * BS;
     UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + P.info) + kvb;
     const int sl = static_cast<int>(U % kRing);
@@ -451,11 +520,36 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
     const int64_t* koff = reinterpret_cast<const int64_t*>(slot + L::koff);
     const int32_t* skpos = reinterpret_cast<const int32_t*>(slot + L::kpos);
     for (int jj = lt; jj < BS; jj += kLoadThreads) kpos[jj] = skpos[jj];
-    // K and V rows alike (lane = 4 dims, converted to bf16), ten of a warp's
-    // rows in flight at a time: rows [0, BS) are K, [BS, 2 BS) V, both
-    // stored [key][128] with the 128-byte swizzle (V is the MMA's MN-major B
-    // operand).
-    {
+    // K and V rows alike (lane = 4 dims, converted to bf16 unless the
+    // operands stay f32), ten of a warp's rows in flight at a time: rows
+    // [0, BS) are K, [BS, 2 BS) V, both stored [key][128] with the 128-byte
+    // swizzle (V is the MMA's MN-major B operand).
+    if constexpr (kTf32) {
+      constexpr int kRows = (2 * BS + kLoaders - 1) / kLoaders;
+#pragma unroll
+      for (int q0 = 0; q0 < kRows; q0 += 10) {
+        float4 kr[10];
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          const int key = r < BS ? r : r - BS;
+          const int64_t off = q0 + q < kRows && r < 2 * BS ? koff[key] : -1;
+          kr[q] = off >= 0 ? __ldg(reinterpret_cast<const float4*>(
+                                 static_cast<const float*>(r < BS ? a.k_pages : a.v_pages) + off) +
+                             lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int r = lw + (q0 + q) * kLoaders;
+          if (q0 + q < kRows && r < 2 * BS) {
+            const int key = r < BS ? r : r - BS;
+            *reinterpret_cast<float4*>((r < BS ? ks : vs) + sw128_offset_f32(BS, key, 4 * lane)) =
+                kr[q];
+          }
+        }
+      }
+    } else {
       constexpr int kRows = (2 * BS + kLoaders - 1) / kLoaders;
 #pragma unroll
       for (int q0 = 0; q0 < kRows; q0 += 10) {
@@ -514,9 +608,9 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
         if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
         return;
       }
-      unsigned char* xq = smem + P.x + static_cast<size_t>(xb) * kM * kD * 2;
+      unsigned char* xq = smem + P.x + static_cast<size_t>(xb) * kM * kD * E;
       int64_t nxt_src = -1;
-      if (a.q16 != nullptr) {
+      if (!kTf32 && a.q16 != nullptr) {
         // bf16 rows (256 bytes): a half-warp per row, 8 dims per lane, two
         // of the warp's rows per load instruction
         constexpr int kPairs = (kRowsPerLoader + 1) / 2;
@@ -546,7 +640,8 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
             *reinterpret_cast<uint4*>(xq + sw128_offset(kM, r, 8 * hl)) = w[i];
         }
       } else {
-        // f32 rows (512 bytes): lane = 4 dims, converted to bf16
+        // f32 rows (512 bytes): lane = 4 dims, converted to bf16 (kept f32
+        // for tf32 operands)
 #pragma unroll
         for (int q0 = 0; q0 < kRowsPerLoader; q0 += kQBatch) {
           float4 v[kQBatch];
@@ -568,9 +663,13 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
 #pragma unroll
           for (int q = 0; q < kQBatch; ++q) {
             const int r = lw + (q0 + q) * kLoaders;
-            if (q0 + q < kRowsPerLoader && r < kM)
-              *reinterpret_cast<uint2*>(xq + sw128_offset(kM, r, 4 * lane)) =
-                  make_uint2(pack_bf16x2_rn(v[q].x, v[q].y), pack_bf16x2_rn(v[q].z, v[q].w));
+            if (q0 + q < kRowsPerLoader && r < kM) {
+              if constexpr (kTf32)
+                *reinterpret_cast<float4*>(xq + sw128_offset_f32(kM, r, 4 * lane)) = v[q];
+              else
+                *reinterpret_cast<uint2*>(xq + sw128_offset(kM, r, 4 * lane)) =
+                    make_uint2(pack_bf16x2_rn(v[q].x, v[q].y), pack_bf16x2_rn(v[q].z, v[q].w));
+            }
           }
         }
       }
@@ -583,30 +682,39 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
 
 // ------------------------------------------------------------------ MMA issue
 
-template <int BS>
+template <int BS, bool kTf32>
 __device__ bool tc_issue_o(unsigned char* smem, const TcPlan& P, const TcBars& B, uint32_t tmem,
                            int kvb, uint32_t T) {
   const int sb = static_cast<int>(T & 1u);
   if (!mbar_wait_bounded(B.p_full + sb, (T >> 1) & 1u)) return false;
   if (T >= 2 && !mbar_wait_bounded(B.o_free + sb, ((T >> 1) - 1) & 1u)) return false;
   tc_fence_after();
-  const uint32_t v_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes + static_cast<size_t>(BS) * kD * 2);
-  const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs) over S's columns
+  constexpr int E = TcCfg<BS, kTf32>::E;
+  const uint32_t v_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes + static_cast<size_t>(BS) * kD * E);
+  const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs, or f32) over S's columns
   const uint32_t t_o = tmem + 256 + 128 * sb;
+  if constexpr (kTf32) {
 #pragma unroll
-  for (int st = 0; st < BS / 16; ++st)   // 16 keys = 2048 bytes of V rows per step
-    mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 2048, BS * 128),
-                idesc_bf16(kM, kD, true), st > 0);
+    for (int st = 0; st < BS / 8; ++st)  // 8 keys = 1024 bytes of V rows per step
+      mma_tf32_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 1024, BS * 128),
+                  idesc_tf32(kM, kD, true), st > 0);
+  } else {
+#pragma unroll
+    for (int st = 0; st < BS / 16; ++st)  // 16 keys = 2048 bytes of V rows per step
+      mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 2048, BS * 128),
+                  idesc_bf16(kM, kD, true), st > 0);
+  }
   mma_commit(B.o_full + sb);
   mma_commit(B.s_free + sb);                     // P read: the S / P columns are free
   return true;
 }
 
-template <int BS>
+template <int BS, bool kTf32>
 __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& P,
                        const TcBars& B, uint32_t tmem) {
-  constexpr int KVB = TcCfg<BS>::KVB;
-  constexpr int kNX = TcCfg<BS>::NX;
+  constexpr int KVB = TcCfg<BS, kTf32>::KVB;
+  constexpr int kNX = TcCfg<BS, kTf32>::NX;
+  constexpr int E = TcCfg<BS, kTf32>::E;
   int64_t* status = a.totals + 3;
   uint32_t T = 0;
   for (uint32_t U = 0;; ++U) {
@@ -630,23 +738,28 @@ __device__ void tc_mma(const ForwardArgs& a, unsigned char* smem, const TcPlan& 
         return;
       }
       tc_fence_after();
-      const uint32_t q_addr = smem_u32(smem + P.x + static_cast<size_t>(xb) * kM * kD * 2);
+      const uint32_t q_addr = smem_u32(smem + P.x + static_cast<size_t>(xb) * kM * kD * E);
       const uint32_t t_s = tmem + 128 * sb;
+      // K steps of 32 bytes (16 bf16 or 8 tf32), four per 128-byte panel
 #pragma unroll
-      for (int st = 0; st < kD / 16; ++st) {
+      for (int st = 0; st < kD * E / 32; ++st) {
         const uint32_t panel = st >> 2;
         const uint32_t kb = (st & 3) * 32;
-        mma_bf16(t_s, sw128_desc(q_addr + panel * kM * 128 + kb),
-                 sw128_desc(k_addr + panel * BS * 128 + kb), idesc_bf16(kM, BS), st > 0);
+        if constexpr (kTf32)
+          mma_tf32(t_s, sw128_desc(q_addr + panel * kM * 128 + kb),
+                   sw128_desc(k_addr + panel * BS * 128 + kb), idesc_tf32(kM, BS), st > 0);
+        else
+          mma_bf16(t_s, sw128_desc(q_addr + panel * kM * 128 + kb),
+                   sw128_desc(k_addr + panel * BS * 128 + kb), idesc_bf16(kM, BS), st > 0);
       }
       mma_commit(B.s_full + sb);
       mma_commit(B.x_empty + xb);                // Q read: the tile buffer is free
-      if (tt > 0 && !tc_issue_o<BS>(smem, P, B, tmem, kvb, T - 1)) {
+      if (tt > 0 && !tc_issue_o<BS, kTf32>(smem, P, B, tmem, kvb, T - 1)) {
         report(status, SA_ERR_DEVICE_TIMEOUT);
         return;
       }
     }
-    if (tiles > 0 && !tc_issue_o<BS>(smem, P, B, tmem, kvb, T - 1)) {
+    if (tiles > 0 && !tc_issue_o<BS, kTf32>(smem, P, B, tmem, kvb, T - 1)) {
       report(status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -702,18 +815,18 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 
 // Softmax warpgroup g (0 or 1) takes the tiles whose running index has
 // parity g, and with them TMEM buffers S[g], O[g].
-template <int BS>
+template <int BS, bool kTf32>
 __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsigned char* smem,
                            const TcPlan& P, const TcBars& B, uint32_t tmem, int warp,
                            int lane) {
   const uint32_t g = static_cast<uint32_t>((warp - 1 - kLoaders) >> 2);
-  constexpr int KVB = TcCfg<BS>::KVB;
+  constexpr int KVB = TcCfg<BS, kTf32>::KVB;
   int64_t* status = a.totals + 3;
   const int row = (warp & 3) * 32 + lane;               // TMEM lane = tile row
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const float qscale = a.scale * kLog2e;
   // the warp's staging tiles (32 rows x 64 bytes each), used in turn
-  constexpr int SB = TcCfg<BS>::SB;
+  constexpr int SB = TcCfg<BS, kTf32>::SB;
   float* const wst0 =
       reinterpret_cast<float*>(smem + P.stage) + (g * 4 + (warp & 3)) * SB * 32 * 16;
   uint32_t rnd = 0;
@@ -909,8 +1022,9 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         }
       }
       const float m2 = any ? ext * qscale : -INFINITY;
-      // pass 2: p = exp(s - m), l, and P as bf16 pairs into the S columns
-      // already read (chunk c's 16 columns lie at or before S chunk c).
+      // pass 2: p = exp(s - m), l, and P into the S columns already read:
+      // bf16 pairs (chunk c's 16 columns lie at or before S chunk c), or, for
+      // tf32 operands, f32 in place of S chunk c.
       const float msub = m2 == -INFINITY ? 0.f : m2;
       const uint64_t qs2 = f32x2(qscale, qscale);
       const uint64_t nm2 = f32x2(-msub, -msub);
@@ -923,7 +1037,15 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         const int cut = jlim - c * 32;
         const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
         const uint32_t live = vmask[c] & inside;
-        uint32_t pk[16];
+        uint32_t pk[kTf32 ? 32 : 16];
+        auto put = [&](int i2, float p0, float p1) {
+          if constexpr (kTf32) {
+            pk[2 * i2] = __float_as_uint(p0);
+            pk[2 * i2 + 1] = __float_as_uint(p1);
+          } else {
+            pk[i2] = pack_bf16x2_rn(p0, p1);
+          }
+        };
         if (live == 0xffffffffu) {
 #pragma unroll
           for (int i2 = 0; i2 < 16; ++i2) {
@@ -932,7 +1054,7 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
             const float p0 = ex2_fast(x0);
             const float p1 = ex2_fast(x1);
             l2 = add_f32x2(l2, f32x2(p0, p1));
-            pk[i2] = pack_bf16x2_rn(p0, p1);
+            put(i2, p0, p1);
           }
         } else {
 #pragma unroll
@@ -943,10 +1065,13 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
             const float p0 = ((live >> i) & 1u) ? ex2_fast(x0) : 0.f;
             const float p1 = ((live >> (i + 1)) & 1u) ? ex2_fast(x1) : 0.f;
             l2 = add_f32x2(l2, f32x2(p0, p1));
-            pk[i2] = pack_bf16x2_rn(p0, p1);
+            put(i2, p0, p1);
           }
         }
-        tmem_st16(t_s + c * 16, pk);
+        if constexpr (kTf32)
+          tmem_st32(t_s + c * 32, pk);
+        else
+          tmem_st16(t_s + c * 16, pk);
       }
       float la, lb;
       f32x2_split(l2, la, lb);
@@ -971,15 +1096,15 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
 
 // ------------------------------------------------------------------ kernel
 
-template <int BS, bool kBf16>
+template <int BS, bool kBf16, bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
 forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
-  constexpr int KVB = TcCfg<BS>::KVB;
-  constexpr int kNX = TcCfg<BS>::NX;
+  constexpr int KVB = TcCfg<BS, kTf32>::KVB;
+  constexpr int kNX = TcCfg<BS, kTf32>::NX;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const TcPlan P = tc_plan(BS);
+  const TcPlan P = tc_plan<BS, kTf32>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   TcBars B;
   B.kv_full = bars;
@@ -1000,6 +1125,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const long long t_start = clock64();
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -1029,11 +1155,14 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
       mbar_init(B.slot_empty + i, kLoadThreads);
     }
     fence_mbar_init();
+    // (a head never has more units than slots; the bound only matters for an
+    // index whose build did not finish)
     int32_t acc = 0;
     for (int hh = 0; hh < a.hkv; ++hh) {
       unit_base[hh] = acc;
-      acc += a.num_sel[hh];
+      acc += static_cast<int32_t>(min(max(static_cast<int64_t>(a.num_sel[hh]), int64_t{0}), a.nbs));
     }
+    if (a.unit_order != nullptr && acc > a.max_units) acc = static_cast<int32_t>(a.max_units);
     unit_base[a.hkv] = acc;
   }
   tc_fence_before();
@@ -1044,16 +1173,16 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
 
   if (warp == 0) {
     if (lane == 0) {
-      tc_mma<BS>(a, smem, P, B, tmem);
+      tc_mma<BS, kTf32>(a, smem, P, B, tmem);
       // Every MMA issued has completed before TMEM is released.
       mma_commit(B.done);
       if (!mbar_wait_bounded(B.done, 0)) report(a.totals + 3, SA_ERR_DEVICE_TIMEOUT);
     }
     __syncwarp();
   } else if (warp <= kLoaders) {
-    tc_loader<BS, kBf16>(a, smem, P, B, warp - 1, lane);
+    tc_loader<BS, kBf16, kTf32>(a, smem, P, B, warp - 1, lane);
   } else if (warp < kSchedWarp) {
-    tc_softmax<BS>(a, &omap, smem, P, B, tmem, warp, lane);
+    tc_softmax<BS, kTf32>(a, &omap, smem, P, B, tmem, warp, lane);
     // box stores issued by this thread have landed before the CTA leaves
     bulk_wait_all();
   } else {
@@ -1063,13 +1192,109 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0 && a.cta_stats != nullptr && static_cast<int>(blockIdx.x) < a.cta_stats_len)
+    a.cta_stats[3 * blockIdx.x + 2] = clock64() - t_start;
 }
 
-template <int BS, bool kBf16>
+// The longest-first work list: every unit (kv head, compact slot) of the
+// index, numbered across heads as the scheduler numbers them, sorted by
+// descending edge count (a counting sort over kOrderBins counts; counts
+// above the last bin share it; equal counts in no particular order, which
+// changes which CTA runs a unit but no result).  One CTA: the list is a
+// few tens of thousands of entries at most.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBins = 2048;
+constexpr int kOrderBatch = 8;     // units whose counts are in flight per thread
+
+__global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a) {
+  __shared__ int32_t ubase[201];
+  __shared__ uint32_t bins[kOrderBins];
+  __shared__ uint32_t warp_tot[kOrderThreads / 32];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int hh = 0; hh < a.hkv; ++hh) {
+      ubase[hh] = acc;
+      acc += static_cast<int32_t>(min(max(static_cast<int64_t>(a.num_sel[hh]), int64_t{0}), a.nbs));
+    }
+    ubase[a.hkv] = acc > a.max_units ? static_cast<int32_t>(a.max_units) : acc;
+  }
+  for (int b = tid; b < kOrderBins; b += kOrderThreads) bins[b] = 0;
+  __syncthreads();
+  const int64_t n = ubase[a.hkv];
+  // bin of unit u: kOrderBins - 1 - min(edges, kOrderBins - 1) (most edges first)
+  auto bins_of = [&](int64_t u0, int (&bin)[kOrderBatch]) {
+    int32_t lo[kOrderBatch], hi[kOrderBatch];
+#pragma unroll
+    for (int q = 0; q < kOrderBatch; ++q) {
+      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
+      lo[q] = hi[q] = 0;
+      if (u < n) {
+        int h = 0;
+        while (h + 1 < a.hkv && ubase[h + 1] <= u) ++h;
+        const int32_t* off = a.sel_offsets + static_cast<int64_t>(h) * (a.nbs + 1) + (u - ubase[h]);
+        lo[q] = off[0];
+        hi[q] = off[1];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kOrderBatch; ++q) {
+      int c = hi[q] - lo[q];
+      c = c < 0 ? 0 : (c > kOrderBins - 1 ? kOrderBins - 1 : c);
+      bin[q] = kOrderBins - 1 - c;
+    }
+  };
+  const int64_t step = static_cast<int64_t>(kOrderThreads) * kOrderBatch;
+  for (int64_t u0 = tid; u0 < n; u0 += step) {
+    int bin[kOrderBatch];
+    bins_of(u0, bin);
+#pragma unroll
+    for (int q = 0; q < kOrderBatch; ++q)
+      if (u0 + static_cast<int64_t>(q) * kOrderThreads < n) atomicAdd(&bins[bin[q]], 1u);
+  }
+  __syncthreads();
+  // exclusive scan of the bins: two per thread, then across the warps
+  constexpr int kPer = kOrderBins / kOrderThreads;
+  uint32_t v[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    v[i] = bins[tid * kPer + i];
+    sum += v[i];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t inc = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += x;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  uint32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  uint32_t run = before + inc - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    bins[tid * kPer + i] = run;
+    run += v[i];
+  }
+  __syncthreads();
+  for (int64_t u0 = tid; u0 < n; u0 += step) {
+    int bin[kOrderBatch];
+    bins_of(u0, bin);
+#pragma unroll
+    for (int q = 0; q < kOrderBatch; ++q) {
+      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
+      if (u < n) a.unit_order[atomicAdd(&bins[bin[q]], 1u)] = static_cast<int32_t>(u);
+    }
+  }
+}
+
+template <int BS, bool kBf16, bool kTf32>
 cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
-  const TcPlan p = tc_plan(BS);
+  const TcPlan p = tc_plan<BS, kTf32>();
   if (p.total > 227 * 1024) return cudaErrorNotSupported;
-  const void* fn = reinterpret_cast<const void*>(forward_tc_kernel<BS, kBf16>);
+  const void* fn = reinterpret_cast<const void*>(forward_tc_kernel<BS, kBf16, kTf32>);
   cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
   if (err != cudaSuccess) return err;
@@ -1096,16 +1321,24 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       args.o_tma = 1;
   }
-  // The work counter starts at zero for every launch.
+  // The work counter starts at zero for every launch, and walks the
+  // longest-first list where the index workspace has room for one.
   if (args.unit_counter != nullptr) {
     const cudaError_t e = cudaMemsetAsync(args.unit_counter, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    args.unit_order = nullptr;
+  }
+  if (args.unit_order != nullptr) {
+    unit_order_kernel<<<1, kOrderThreads, 0, stream>>>(args);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // One CTA per SM: it holds all 512 TMEM columns.
   int64_t grid = device_sm_count();
   if (grid > a.max_splits) grid = a.max_splits;
   if (grid < 1) grid = 1;
-  forward_tc_kernel<BS, kBf16>
+  forward_tc_kernel<BS, kBf16, kTf32>
       <<<static_cast<unsigned>(grid), kThreads, p.total, stream>>>(omap, args);
   return cudaGetLastError();
 }
@@ -1150,9 +1383,14 @@ bool forward_tc_supported(int head_dim, int block_size, int page_size, int qhead
 cudaError_t launch_forward_tc(const ForwardArgs& a, cudaStream_t stream) {
   if (!forward_tc_supported(a.head_dim, a.block_size, a.page_size, a.qhead) || a.hkv > 200)
     return cudaErrorNotSupported;
-  if (a.block_size == 64)
-    return a.kv_bf16 ? launch_tc<64, true>(a, stream) : launch_tc<64, false>(a, stream);
-  return a.kv_bf16 ? launch_tc<128, true>(a, stream) : launch_tc<128, false>(a, stream);
+  // tf32 operands only for f32 K/V (bf16 K/V are exact in bf16)
+  const bool tf32 = a.tf32 && !a.kv_bf16;
+  if (a.block_size == 64) {
+    if (a.kv_bf16) return launch_tc<64, true, false>(a, stream);
+    return tf32 ? launch_tc<64, false, true>(a, stream) : launch_tc<64, false, false>(a, stream);
+  }
+  if (a.kv_bf16) return launch_tc<128, true, false>(a, stream);
+  return tf32 ? launch_tc<128, false, true>(a, stream) : launch_tc<128, false, false>(a, stream);
 }
 
 }  // namespace sa

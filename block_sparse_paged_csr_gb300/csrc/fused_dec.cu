@@ -115,6 +115,7 @@ __host__ __device__ constexpr Layout fused_layout() {
 }
 
 struct Smem {
+  uint32_t spin;        // tries of every mbarrier wait
   unsigned char* base;
   float* qs;
   StageHdr* hdr;
@@ -155,7 +156,7 @@ __device__ void meta_warp(const FusedDecArgs& a, const Smem& sm, int64_t n_piece
   for (int64_t g = blockIdx.x;; g += gridDim.x, ++n) {
     const int slot = static_cast<int>(n % kDescs);
     if (n >= static_cast<uint32_t>(kDescs) &&
-        !mbar_wait_bounded(sm.dempty + slot, ((n / kDescs) - 1) & 1u)) {
+        !mbar_wait_bounded(sm.dempty + slot, ((n / kDescs) - 1) & 1u, sm.spin)) {
       if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -193,14 +194,11 @@ __device__ void meta_warp(const FusedDecArgs& a, const Smem& sm, int64_t n_piece
       int blk = 0;
       if (jr < nrange) {
         const int r = r0 + jr;
-        kept = a.inv[(static_cast<int64_t>(h) * a.tq + i) * a.topk + r] >= 0;
-        if (kept) {
-          blk = a.selected[(i * a.hkv + h) * a.topk + r];
-          if (blk < 0 || blk >= a.msb) {    // only after an index that reported an error
-            report(a.status, SA_ERR_SELECTED_RANGE);
-            kept = false;
-          }
-        }
+        // the index's rule for keeping an entry (its inv >= 0): a block id in
+        // [0, msb) whose first key lies below the sequence's KV length
+        blk = a.selected[(i * a.hkv + h) * a.topk + r];
+        if (blk < -1 || blk >= a.msb) report(a.status, SA_ERR_SELECTED_RANGE);
+        kept = blk >= 0 && blk < a.msb && static_cast<int64_t>(blk) * a.block_size < lk;
       }
       const unsigned km = __ballot_sync(0xffffffffu, kept);
       if (kept) {
@@ -254,9 +252,10 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
   const uint32_t q_bytes = static_cast<uint32_t>(a.qhead) * kD * 4;
   uint32_t n = 0, xs = 0;
   bool ok = true;
+  if (a.stall) return;   // test hook: no stage is ever filled, so every wait on one runs out
   for (;;) {
     const int slot = static_cast<int>(n % kDescs);
-    if (!mbar_wait_bounded(sm.dfull + slot, (n / kDescs) & 1u)) {
+    if (!mbar_wait_bounded(sm.dfull + slot, (n / kDescs) & 1u, sm.spin)) {
       ok = false;
       break;
     }
@@ -265,7 +264,7 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
     if (item < 0) {
       if (xs % NL != static_cast<uint32_t>(lw)) break;   // another load warp ends the ring
       const int s = static_cast<int>(xs % S);
-      if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u)) {
+      if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u, sm.spin)) {
         ok = false;
         break;
       }
@@ -285,7 +284,7 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
       }
       const int j = u / cpb, c = u - j * cpb;
       const int s = static_cast<int>(xs % S);
-      if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u)) {
+      if (xs >= static_cast<uint32_t>(S) && !mbar_wait_bounded(sm.empty + s, ((xs / S) - 1) & 1u, sm.spin)) {
         ok = false;
         break;
       }
@@ -359,7 +358,7 @@ __device__ void load_warp(const TmaMaps& maps, const FusedDecArgs& a, const Smem
     if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
     // Let this warp's copies still in flight land before the CTA can exit.
     for (uint32_t x = xs > static_cast<uint32_t>(S) ? xs - S : 0u; x < xs; ++x)
-      if (x % NL == static_cast<uint32_t>(lw)) mbar_wait_bounded(sm.full + x % S, (x / S) & 1u);
+      if (x % NL == static_cast<uint32_t>(lw)) mbar_wait_bounded(sm.full + x % S, (x / S) & 1u, sm.spin);
   }
 }
 
@@ -395,7 +394,7 @@ template <int NC, int R>
 __device__ void merge_warp(const FusedDecArgs& a, const Smem& sm, int lane) {
   const int qhead = a.qhead;
   for (uint32_t np = 0;; ++np) {
-    if (!mbar_wait_bounded(sm.mready, np & 1u)) {
+    if (!mbar_wait_bounded(sm.mready, np & 1u, sm.spin)) {
       if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -505,7 +504,7 @@ __device__ void merge_warp(const FusedDecArgs& a, const Smem& sm, int lane) {
 // Consumer side of a piece's end: wait until the merge warp has read the
 // previous piece's states (bounded), then the caller writes its state.
 __device__ __forceinline__ bool handoff_wait(const Smem& sm, uint32_t handed) {
-  return handed == 0 || mbar_wait_bounded(sm.mfree, (handed - 1) & 1u);
+  return handed == 0 || mbar_wait_bounded(sm.mfree, (handed - 1) & 1u, sm.spin);
 }
 
 // After the caller's state is written: consumer 0 names the piece, every
@@ -547,7 +546,7 @@ __device__ void consumer_f32(const FusedDecArgs& a, const Smem& sm, int w, int l
   uint32_t xc = 0, handed = 0;
   for (;;) {
     const int s = static_cast<int>(xc % S);
-    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
+    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u, sm.spin)) {
       if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -719,7 +718,7 @@ __device__ void consumer_bf16(const FusedDecArgs& a, const Smem& sm, int w, int 
   uint32_t xc = 0, handed = 0;
   for (;;) {
     const int s = static_cast<int>(xc % S);
-    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
+    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u, sm.spin)) {
       if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -895,7 +894,7 @@ __device__ void consumer_bf16_packed(const FusedDecArgs& a, const Smem& sm, int 
   uint32_t xc = 0, handed = 0;
   for (;;) {
     const int s = static_cast<int>(xc % S);
-    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u)) {
+    if (!mbar_wait_bounded(sm.full + s, (xc / S) & 1u, sm.spin)) {
       if (lane == 0) report(a.status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -1031,6 +1030,7 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Smem sm;
+  sm.spin = a.spin_limit ? a.spin_limit : kSpinLimit;
   sm.base = base;
   sm.qs = reinterpret_cast<float*>(base + L.q);
   sm.hdr = reinterpret_cast<StageHdr*>(base + L.hdr);
@@ -1082,6 +1082,9 @@ fused_dec_kernel(const __grid_constant__ TmaMaps maps, const FusedDecArgs a) {
   } else {
     consumer_f32<R, S>(a, sm, warp - NL - 2, lane);
   }
+  // Launched behind the index kernel (programmatic dependent launch): finish
+  // only after it, so that later work of the stream sees both complete.
+  if (a.pdl) griddep_wait();
 }
 
 // ------------------------------------------------------------------ host
@@ -1172,9 +1175,21 @@ cudaError_t launch_fused(const FusedDecArgs& a, cudaStream_t stream) {
   int64_t grid = device_sm_count();
   if (grid > n_pieces) grid = n_pieces;
   if (grid < 1) return cudaSuccess;
-  fused_dec_kernel<kBf16, R, S>
-      <<<static_cast<unsigned>(grid), (2 + NL + NC) * 32, smem, stream>>>(maps, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3((2 + NL + NC) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  FusedDecArgs args = a;
+  int site = kStallNone;
+  debug_stall_setting(&site, &args.spin_limit);
+  args.stall = site == kStallFusedCopies;
+  return cudaLaunchKernelEx(&cfg, fused_dec_kernel<kBf16, R, S>, maps, args);
 }
 
 }  // namespace

@@ -58,7 +58,8 @@ __device__ __forceinline__ int64_t splits_of(int64_t count, int split_edges) {
 // runs `last` (with all of its threads), then resets the counter and bumps the
 // generation; the others spin (bounded) on the generation.
 template <typename F>
-__device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, F last) {
+__device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, uint32_t limit,
+                             bool stall, F last) {
   __shared__ int s_ok, s_last;
   __shared__ uint32_t s_gen;
   __syncthreads();
@@ -67,6 +68,7 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, F
     s_gen = ld_acquire_u32(gen);
     __threadfence();
     s_last = atomicAdd(count, 1u) == nblocks - 1;
+    if (stall) s_last = 0;   // test hook: nobody releases the barrier
   }
   __syncthreads();
   if (s_last) {
@@ -81,7 +83,7 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, F
   } else if (threadIdx.x == 0) {
     uint32_t it = 0;
     while (ld_acquire_u32(gen) == s_gen) {
-      if (++it > kSpinLimit) {
+      if (++it > limit) {
         s_ok = 0;
         break;
       }
@@ -199,23 +201,45 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   const int nseg = a.hkv * batch;
 
   // ---- chunk table (every CTA builds its own copy) -------------------------
-  if (tid == 0) {
-    int32_t c = 0, m = 0;
-    for (int b = 0; b < batch; ++b) {
-      chunk_base[b] = c;
-      multi_base[b] = m;
-      const int64_t n = (a.cu[b + 1] - a.cu[b]) * topk;
-      const int32_t nc = static_cast<int32_t>((n + kChunkEntries - 1) / kChunkEntries);
-      c += nc;
-      if (nc > 1) m += nc;
+  // chunk_base[b]: chunks of the sequences before b; multi_base[b]: the same
+  // over sequences of several chunks.  One block scan per kThreads sequences
+  // (the cu reads of a tile are issued together, not one after another).
+  {
+    int64_t carry_c = 0, carry_m = 0;
+    for (int base = 0; base < batch; base += kThreads) {
+      const int b = base + tid;
+      int64_t v[3] = {0, 0, 0};
+      if (b < batch) {
+        const int64_t n = (a.cu[b + 1] - a.cu[b]) * topk;
+        const int64_t nc = (n + kChunkEntries - 1) / kChunkEntries;
+        v[0] = nc;
+        v[1] = nc > 1 ? nc : 0;
+      }
+      int64_t excl[3], tot[3];
+      block_scan3(v, excl, tot, s.scratch);
+      if (b < batch) {
+        chunk_base[b] = static_cast<int32_t>(carry_c + excl[0]);
+        multi_base[b] = static_cast<int32_t>(carry_m + excl[1]);
+      }
+      carry_c += tot[0];
+      carry_m += tot[1];
     }
-    chunk_base[batch] = c;
-    multi_base[batch] = m;
-    s.nch_head = c;
-    s.nmulti_head = m;
+    if (tid == 0) {
+      chunk_base[batch] = static_cast<int32_t>(carry_c);
+      multi_base[batch] = static_cast<int32_t>(carry_m);
+      s.nch_head = static_cast<int32_t>(carry_c);
+      s.nmulti_head = static_cast<int32_t>(carry_m);
+    }
   }
-  if (blockIdx.x == 0 && tid == 0) *status = 0;
+  if (blockIdx.x == 0 && tid == 0) {
+    *status = 0;
+    __threadfence();
+  }
   __syncthreads();
+  // A fused decode kernel launched behind this one reads none of its outputs
+  // (only the memset workspace counters and the status word cleared above):
+  // let it start now.
+  griddep_launch_dependents();
   const int nch_head = s.nch_head;
   const int nmulti = s.nmulti_head;
 
@@ -314,7 +338,8 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
       for (int j = 0; j < 3; ++j) seg_pre[3 * nseg + j] = carry[j];
     __threadfence();
   };
-  if (!grid_barrier(bar_count, bar_gen, gridDim.x, scan_segments)) {
+  if (!grid_barrier(bar_count, bar_gen, gridDim.x, a.spin_limit ? a.spin_limit : kSpinLimit,
+                    a.stall != 0, scan_segments)) {
     if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
     return;
   }
@@ -547,6 +572,19 @@ WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
   return L;
 }
 
+LptRegion lpt_region(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32_t msb,
+                     int64_t nbs) {
+  const size_t build = workspace_layout(hkv, batch, tq, index_hist_slot_bound(tq, topk), msb).total;
+  const int64_t entries = tq * hkv * static_cast<int64_t>(topk);
+  const int64_t slots = static_cast<int64_t>(hkv) * nbs;
+  const int64_t units = entries < slots ? entries : slots;
+  LptRegion r;
+  r.units = units > 0 ? units : 1;
+  r.offset = (build + 255) & ~static_cast<size_t>(255);
+  r.bytes = (4 * static_cast<size_t>(units > 0 ? units : 1) + 255) & ~static_cast<size_t>(255);
+  return r;
+}
+
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
                                int64_t hist_slots_per_head, cudaStream_t stream) {
   const WorkspaceLayout lay =
@@ -570,6 +608,9 @@ cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
   const int64_t want = std::max<int64_t>(std::max<int64_t>(n_chunks, plateau_ctas), 1);
   if (grid > want) grid = want;
   IndexArgs args = a;
+  int site = kStallNone;
+  debug_stall_setting(&site, &args.spin_limit);
+  args.stall = site == kStallIndexBarrier;
   WorkspaceLayout layout = lay;
   int64_t nch = n_chunks;
   void* params[] = {&args, &layout, &nch};

@@ -30,11 +30,29 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
                                  int64_t hist_slots_per_head, int32_t msb);
+
+// The tensor-core forward's longest-first work list in the index workspace,
+// after everything an index build of these sizes may use: `offset` bytes
+// from the workspace start, `bytes` long (int32 per possible work unit).
+struct LptRegion {
+  size_t offset, bytes;
+  int64_t units;
+};
+LptRegion lpt_region(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32_t msb,
+                     int64_t nbs);
 // Chunks of one head (and, in *multi_slots, chunks of its multi-chunk segments).
 int64_t index_chunks_per_head(const int64_t* cu_host, int32_t batch, int32_t topk,
                               int64_t* multi_slots);
 // Upper bound of the multi-chunk histogram slots of one head.
 int64_t index_hist_slot_bound(int64_t tq, int32_t topk);
+
+// Test hook (sa_debug_stall): a site whose bounded wait is made to run out,
+// and the tries a bounded wait takes before it gives up (0 = kSpinLimit).
+enum StallSite { kStallNone = 0, kStallIndexBarrier = 1, kStallFusedCopies = 2 };
+void debug_stall_setting(int* site, uint32_t* spin_limit);
+// Test hook (sa_debug_cta_stats): where the tensor-core forward adds up each
+// CTA's rows, units and busy cycles (NULL: nowhere), and its length in CTAs.
+void debug_cta_stats(int64_t** buf, int32_t* n_ctas);
 
 struct IndexArgs {
   const int32_t* selected;
@@ -44,6 +62,8 @@ struct IndexArgs {
   int32_t hkv, topk, batch, msb, block_size, split_edges;
   int64_t nbs;
   sa_index idx;             // output arrays + workspace
+  uint32_t spin_limit;      // tries of the grid barrier's wait (0 = kSpinLimit)
+  int stall;                // test hook: the grid barrier is never released
 };
 
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
@@ -76,8 +96,15 @@ struct ForwardArgs {
   int o_bf16;
   int o_tma;                // set by a launcher: o rows may go out by tensor-map stores
   const uint16_t* q16;      // nullable: Q rounded to bf16, same layout (tensor-core kernel)
+  int tf32;                 // tensor-core kernel: f32 K/V as tf32 operands (else bf16)
   uint32_t* unit_counter;   // nullable: the tensor-core kernel's work counter (in the
                             // index workspace; cleared by its launcher)
+  int32_t* unit_order;      // nullable: room for one int32 per possible unit (in the
+                            // index workspace): the launcher writes the units there in
+                            // longest-first order and the counter walks that list
+  int64_t max_units;        // entries unit_order has room for
+  int64_t* cta_stats;       // nullable (test hook): per CTA rows, units, busy cycles
+  int32_t cta_stats_len;    // CTAs cta_stats has room for
   float* m_partial;
   float* l_partial;
 };
@@ -130,6 +157,11 @@ struct FusedDecArgs {
   float* part_l;
   float* out;
   float* lse;               // nullable
+  int pdl;                  // launched right behind the index kernel that built the
+                            // index: it may start while that kernel runs (it reads
+                            // nothing the index writes) and waits for it at its end
+  uint32_t spin_limit;      // tries of every mbarrier wait (0 = kSpinLimit)
+  int stall;                // test hook: the load warps issue no copy at all
 };
 
 // Whether the fused decode kernel supports this shape (the caller also checks

@@ -21,6 +21,19 @@ __device__ __forceinline__ void report(int64_t* status_word, int code) {
               static_cast<unsigned long long>(code));
 }
 
+// Programmatic dependent launch: a kernel lets the next kernel of its stream
+// (launched with programmatic stream serialization) start before it ends;
+// that kernel waits for its prerequisite grids to finish, and their memory to
+// be visible, where it calls griddep_wait.  Both are no-ops without such a
+// launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -63,9 +76,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, at most kSpinLimit tries.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Wait for phase `parity` of `bar` to complete, at most `limit` tries
+// (kSpinLimit by default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -140,6 +155,13 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // have read their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// All but the N most recent of the issuing thread's committed bulk stores
+// have read their shared-memory sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 // The issuing thread's committed bulk stores have completed.

@@ -71,14 +71,19 @@ typedef enum sa_path {
                                     problems with bf16 K/V use warp-level MMA (Q and
                                     P split into two bf16 parts); others use the
                                     tcgen05 kernel (block 64 or 128, qhead dividing
-                                    128, bf16 operands); f32 accumulation;
+                                    128): bf16 operands for bf16 K/V, tf32 operands
+                                    (Q, K, V and P kept in f32 in shared and tensor
+                                    memory) for f32 K/V; f32 accumulation;
                                     SA_ERR_UNSUPPORTED elsewhere                   */
   SA_PATH_CUDA_CORE_GENERAL = 3, /* the general f32 FMA kernel only                 */
-  SA_PATH_FUSED_DECODE = 4       /* sa_attention / sa_forward_combine only: forward
+  SA_PATH_FUSED_DECODE = 4,      /* sa_attention / sa_forward_combine only: forward
                                     and combine as one kernel when every sequence
                                     holds at most one query (see sa_attention);
                                     SA_ERR_UNSUPPORTED elsewhere and from
                                     sa_forward                                   */
+  SA_PATH_TENSOR_CORE_BF16 = 5   /* as SA_PATH_TENSOR_CORE, but the tcgen05 kernel
+                                    rounds f32 K/V, Q and P to bf16 operands too
+                                    (half the shared-memory bytes of tf32; looser) */
 } sa_path;
 
 /*
@@ -266,13 +271,18 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * SA_ERR_UNSUPPORTED.  SA_PATH_AUTO sends decode-shaped problems (tq at most
  * twice the batch) to the pipelined CUDA-core kernel (f32 K/V) or to the
  * warp-level MMA kernel (bf16 K/V), and the others to the tcgen05 kernel
- * where supported (operands rounded to bf16; use SA_PATH_CUDA_CORE for f32
- * arithmetic throughout).  The tcgen05 kernel claims work units from a
+ * where supported (tf32 operands for f32 K/V, bf16 for bf16 K/V; use
+ * SA_PATH_CUDA_CORE for f32 arithmetic throughout, SA_PATH_TENSOR_CORE_BF16
+ * for bf16 operands with f32 K/V).  The tcgen05 kernel claims work units from a
  * counter in the first 256 bytes of the index's scratch (cleared on the
  * stream before each launch): idx->workspace when it is set and
  * idx->workspace_bytes is at least 256, the library's array for an index
- * with SA_INDEX_STATIC_SCRATCH; with neither it takes units round-robin.  So
- * one index serves one forward at a time.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
+ * with SA_INDEX_STATIC_SCRATCH; with neither it takes units round-robin.
+ * When that scratch also has room for the work list that follows the build's
+ * own use of it (sa_index_query_sizes counts it in workspace_bytes), a
+ * one-CTA kernel first sorts the units by descending edge count and the
+ * counter walks that longest-first list.  So one index serves one forward
+ * at a time.  Checks: HEAD_COUNT, BLOCK_PAGE, SHAPE (idx geometry),
  * UNSUPPORTED, INVALID_ARGUMENT; on device: SHAPE (page id >= num_pages).
  */
 sa_status sa_forward(const float *q, const void *k_pages, const void *v_pages,
@@ -439,6 +449,39 @@ sa_status sa_attention_ex(const float *q, const void *k_pages, const void *v_pag
                           int32_t causal, int32_t split_edges, sa_index *idx,
                           sa_dtype partial_dtype, void *o_partial, float *m_partial,
                           float *l_partial, float *out, float *lse, sa_path path, void *stream);
+
+/*
+ * Test hook for the bounded device waits (the pages have no counterpart:
+ * their GpuRuntimeError stands for any device failure).  Every wait inside
+ * the kernels gives up after a bounded number of tries, records
+ * SA_ERR_DEVICE_TIMEOUT in the index's status word and lets the kernel
+ * return.  This call makes one such wait run out on purpose, so that a test
+ * can see the status and then check that the next clean call works:
+ *   site 1: the index kernel's grid barrier is never released (every CTA of
+ *           the build times out and returns; the index is left unfinished);
+ *   site 2: the fused decode kernel's load warps issue no copy (its
+ *           consumer, merge and metadata warps time out and return; no copy
+ *           is ever in flight);
+ *   site 0: normal operation.
+ * spin_limit: tries of each bounded wait from now on (0 = the library's
+ * default, about a second).  Process-wide, read at every launch; not for
+ * production use and not safe to change while other threads launch.
+ * Returns SA_ERR_INVALID_ARGUMENT for an unknown site.
+ */
+sa_status sa_debug_stall(int32_t site, uint32_t spin_limit);
+
+/*
+ * Test hook for the tensor-core forward's load balance (the pages have no
+ * counterpart: their WorkSplit list is walked by a thread pool).  With
+ * n_ctas > 0, every later tcgen05 forward adds, for each CTA c < n_ctas,
+ * the rows (edge x GQA lane) and the units it claimed to stats[3 c] and
+ * stats[3 c + 1], and writes the CTA's busy time in SM clock cycles (kernel
+ * start to end) to stats[3 c + 2].  stats: device memory of 3 * n_ctas
+ * int64 that the caller zeroes; n_ctas = 0 turns the hook off.
+ * Process-wide, not for production use.  SA_ERR_INVALID_ARGUMENT for
+ * n_ctas < 0 or a NULL stats with n_ctas > 0.
+ */
+sa_status sa_debug_cta_stats(int64_t *stats, int32_t n_ctas);
 
 /* Synchronises `stream` and returns the first device-detected error recorded
  * in idx->totals[3] (SA_OK if none), or SA_ERR_CUDA if the stream failed. */
