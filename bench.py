@@ -397,6 +397,25 @@ def measure_workload(name, args, rank, world, local_rank):
     st = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])
     index_ms, fwd_ms, comb_ms = (float(x) for x in st.mean(axis=0))
 
+    # f32 K/V on the tensor-core kernel: bf16 operands by default; the
+    # opt-in tf32 scores are timed beside them (forward stage only)
+    tf32_scores = None
+    if fwd_kernel == "forward_tc_kernel" and w.kv_dtype == "f32":
+        eb = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_stage)]
+        for s_ in range(n_stage):
+            flush.fill_(float(s_))
+            eb[s_][0].record(stream)
+            sa.sa_forward(q, k, v, index, bt, cu, used, w.hq, w.hkv, w.head_dim, w.block_size,
+                          w.page_size, w.softmax_scale, w.causal, o_p, m_p, l_p, q_scratch=out,
+                          path=sa.PATH_TENSOR_CORE_TF32)
+            eb[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+        bms = float(np.mean([x[0].elapsed_time(x[1]) for x in eb]))
+        tf32_scores = {"forward_ms": bms,
+                       "roofline_frac": acct["forward"] / (bms / 1e3) / 1e9 / measured_peak()[0],
+                       "note": "sa_forward with SA_PATH_TENSOR_CORE_TF32 (S = Q K^T from f32 Q "
+                               "and K as tf32 operands, P and V bf16)"}
+
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
     if not args.no_e2e:
@@ -487,13 +506,15 @@ def measure_workload(name, args, rank, world, local_rank):
                      "frac": fwd_gbs / peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": acct["forward"],
                      "traffic": traffic},
+        "tensor_core_operands": "bf16" if fwd_kernel == "forward_tc_kernel" else None,
+        "tf32_scores": tf32_scores,
         "algorithmic_bytes": {k_: acct[k_] for k_ in ("kv", "q", "partials_write", "out",
                                                        "step", "forward", "combine")},
         "edges": acct["edges"],
         "e2e": e2e,
         # library kernels per step: the index kernel, then the fused decode
         # kernel, or forward + combine (the tensor-core forward preceded by
-        # the pass that rounds Q to bf16 into its scratch and by the one that
+        # the pass that rounds Q to bf16 into its scratch and the one that
         # sorts its units longest-first)
         "gpu_launches": (2 if fused else (5 if fwd_kernel == "forward_tc_kernel" else 3))
                         * args.steps,

@@ -26,14 +26,14 @@ import torch
 
 from . import _native
 from ._native import (DTYPE_BF16, DTYPE_F32, PATH_AUTO, PATH_CUDA_CORE, PATH_CUDA_CORE_GENERAL,
-                      PATH_FUSED_DECODE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_BF16, STATUS_NAMES)
+                      PATH_FUSED_DECODE, PATH_TENSOR_CORE, PATH_TENSOR_CORE_TF32, STATUS_NAMES)
 
 __all__ = ["SAError", "Index", "sa_index_query_sizes", "sa_build_index",
            "sa_build_index_no_alloc", "sa_forward", "sa_forward_combine", "sa_forward_kernel_name",
            "sa_attention_kernel_name", "PATH_FUSED_DECODE",
            "sa_combine", "sa_attention", "sa_get_status", "sa_clear_status", "sa_status_string",
            "sa_version", "allocate_index", "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
-           "PATH_TENSOR_CORE_BF16",
+           "PATH_TENSOR_CORE_TF32",
            "PATH_CUDA_CORE_GENERAL", "AttentionGraph", "sa_debug_stall", "sa_debug_cta_stats", "STALL_NONE",
            "STALL_INDEX_BARRIER", "STALL_FUSED_COPIES"]
 

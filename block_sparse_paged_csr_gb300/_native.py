@@ -16,7 +16,7 @@ STATUS_NAMES = {
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL, PATH_FUSED_DECODE = 0, 1, 2, 3, 4
-PATH_TENSOR_CORE_BF16 = 5
+PATH_TENSOR_CORE_TF32 = 5
 
 #: Every symbol include/sa.h declares.
 EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",

@@ -1,6 +1,7 @@
 // C ABI of libsa (declared in include/sa.h): argument checks in the order of
 // kvouter_forward's "argument sanity" (forward.rs) and of the error enum
 // (types.rs), then kernel launches on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -80,7 +81,7 @@ FwdKernel choose_forward(int64_t tq, int32_t batch, int32_t qhead, int32_t head_
   const bool cc_ok = sa::forward_cc_supported(head_dim, block_size, kv_bf16);
   switch (path) {
     case SA_PATH_TENSOR_CORE:
-    case SA_PATH_TENSOR_CORE_BF16:
+    case SA_PATH_TENSOR_CORE_TF32:
       if (decode_like && mma_ok) return FwdKernel::kDecodeMma;
       return tc_ok ? FwdKernel::kTensor : FwdKernel::kNone;
     case SA_PATH_CUDA_CORE:
@@ -256,6 +257,12 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   a.split_edges = split_edges;
   a.nbs = nbs;
   a.idx = *idx;
+  // decode batches (every (kv head, sequence) segment of at most 64 entries)
+  // take the kernel's warp-per-segment mode
+  int64_t longest = 0;
+  for (int32_t b = 0; b < batch; ++b)
+    longest = std::max<int64_t>(longest, cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b]);
+  a.small = longest * topk <= sa::kSmallSegment ? 1 : 0;
   const cudaError_t err =
       sa::launch_build_index(a, chunks_per_head, multi_slots, static_cast<cudaStream_t>(stream));
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
@@ -307,7 +314,7 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
   const int kv_bf16 = kv_dtype == SA_DTYPE_BF16 ? 1 : 0;
   if (path == SA_PATH_FUSED_DECODE) return SA_ERR_UNSUPPORTED;   // writes no partials
   if (path != SA_PATH_AUTO && path != SA_PATH_CUDA_CORE && path != SA_PATH_CUDA_CORE_GENERAL &&
-      path != SA_PATH_TENSOR_CORE && path != SA_PATH_TENSOR_CORE_BF16)
+      path != SA_PATH_TENSOR_CORE && path != SA_PATH_TENSOR_CORE_TF32)
     return SA_ERR_INVALID_ARGUMENT;
   const FwdKernel kernel = choose_forward(idx->tq, idx->batch, hq / hkv, head_dim, block_size,
                                           page_size, kv_bf16, path);
@@ -367,8 +374,8 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
     }
   }
   if (kernel == FwdKernel::kTensor) sa::debug_cta_stats(&a.cta_stats, &a.cta_stats_len);
-  // f32 K/V stay f32 (tf32 operands) unless bf16 operands are asked for
-  a.tf32 = kernel == FwdKernel::kTensor && !kv_bf16 && path != SA_PATH_TENSOR_CORE_BF16;
+  // tf32 scores for f32 K/V where asked for; bf16 operands otherwise
+  a.tf32 = kernel == FwdKernel::kTensor && !kv_bf16 && path == SA_PATH_TENSOR_CORE_TF32;
   if (kernel == FwdKernel::kTensor && !a.tf32 && q16_scratch != nullptr) {
     const int64_t n = idx->tq * static_cast<int64_t>(hq) * head_dim;
     err = sa::launch_q_to_bf16(q, static_cast<uint16_t*>(q16_scratch), n, s);
@@ -658,7 +665,7 @@ sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pag
     if (path == SA_PATH_FUSED_DECODE && !fused) return SA_ERR_UNSUPPORTED;
   }
   if (!fused && !sa::forward_cc_supported(head_dim, block_size, kv_bf16) &&
-      !((path == SA_PATH_TENSOR_CORE || path == SA_PATH_TENSOR_CORE_BF16) &&
+      !((path == SA_PATH_TENSOR_CORE || path == SA_PATH_TENSOR_CORE_TF32) &&
         sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv)))
     return SA_ERR_UNSUPPORTED;
   const sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q,

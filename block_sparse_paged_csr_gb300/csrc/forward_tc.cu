@@ -53,7 +53,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;            // rows per MMA tile
-constexpr int kThreads = 768;   // MMA warp, 14 loader warps, 2 x 4 softmax warps, scheduler
+constexpr int kThreads = 640;   // MMA warp, scheduler, 10 loader warps, 2 x 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // S[2] at columns 0 / 128, O[2] at 256 / 384
@@ -114,15 +114,30 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// D (TMEM) (+)= A (TMEM, row i in lane i, one tf32 per column) x B (smem)^T.
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// 64 consecutive f32 columns of this thread's TMEM lane (one round trip).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+        "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+        "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+        "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
       : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 32 consecutive 32-bit columns of this thread's TMEM lane.
@@ -250,24 +265,33 @@ __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off
   }
 }
 
-constexpr int kLoaders = 14;         // loader warps 1..14
+constexpr int kLoaders = 10;         // loader warps 2..11
 constexpr int kLoadThreads = 32 * kLoaders;
 constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 10
 constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
+constexpr int kKvBatch = 13;              // K/V rows in flight per loader warp
 
-// kTf32: operands kept in f32 (tcgen05 kind::tf32) instead of rounded to
-// bf16; every shared-memory tile is then twice as large.
+// kTf32: the scores S = Q K^T from Q and K kept in f32 (tcgen05 kind::tf32)
+// instead of rounded to bf16, so their Q and K tiles are twice as large; P
+// and V stay bf16 operands of O = P V either way.
 template <int BS, bool kTf32 = false> struct TcCfg {
-  static constexpr int E = kTf32 ? 4 : 2;         // bytes per operand element
+  static constexpr int E = kTf32 ? 4 : 2;         // bytes per Q / K element
   static constexpr int KVB = kTf32 && BS == 128 ? 1 : 2;     // unit buffers (K, V)
-  static constexpr int NX = kTf32 ? 1 : (BS == 128 ? 2 : 3); // tile buffers (Q)
+  static constexpr int NX = kTf32 || BS == 128 ? 1 : 3;     // tile buffers (Q)
   // epilogue staging tiles per warp: two where shared memory allows (the
   // box store of one drains while the other fills)
-  static constexpr int SB = !kTf32 && BS == 64 ? 2 : 1;
+  static constexpr int SB = kTf32 && BS == 128 ? 1 : 2;
 };
 constexpr int kMaxNX = 3;
 constexpr int kRing = 4;                          // unit slots of the scheduler
-constexpr int kSchedWarp = 1 + kLoaders + 8;      // warp 23
+// Warp roles: 0 MMA issue, 1 scheduler, 2..11 loaders, 12..19 softmax and
+// epilogue (two warpgroups; warp w reads TMEM lanes 32 (w % 4) ..).  640
+// threads leave 96 registers to each, room for 64 TMEM columns per load.
+constexpr int kSchedWarp = 1;
+constexpr int kLoaderWarp0 = 2;
+constexpr int kSoftmaxWarp0 = kLoaderWarp0 + kLoaders;   // 12
+static_assert(kSoftmaxWarp0 % 4 == 0 && kSoftmaxWarp0 * 32 + 8 * 32 == kThreads,
+              "softmax warpgroups aligned to TMEM lane quarters");
 
 struct UnitInfo {
   int32_t rows;         // edges x qhead of the unit (0: skip)
@@ -309,7 +333,7 @@ __host__ __device__ inline TcPlan tc_plan() {
   using C = TcCfg<BS, kTf32>;
   const int bs = BS, kvb = C::KVB, nx = C::NX, sb = C::SB;
   TcPlan p{};
-  p.kv_bytes = static_cast<size_t>(bs) * kD * C::E * 2;
+  p.kv_bytes = static_cast<size_t>(bs) * kD * (C::E + 2);               // K, then V (bf16)
   p.kv = 0;                                                             // 1024-aligned
   p.x = p.kv + kvb * p.kv_bytes;                                        // [nx] Q tiles
   p.kpos = tc_up(p.x + nx * static_cast<size_t>(kM) * kD * C::E, 128);  // int32 [kvb][BS]
@@ -371,6 +395,25 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
   const int qhead = a.qhead;
   const int ps = a.page_size;
   int64_t* status = a.totals + 3;
+  // The next unit: claimed from the forward's counter (whichever CTA is free
+  // takes the next unit in index order, so heavy units of a skewed selection
+  // do not pile up on a few CTAs), or round-robin without one.  With a
+  // longest-first list the counter walks that list instead.  Each claim is
+  // made one unit ahead, so its round trips overlap the current unit's.
+  auto claim = [&](uint32_t U) -> int64_t {
+    int64_t c = 0;
+    if (lane == 0) {
+      if (a.unit_counter != nullptr) {
+        const uint32_t k = atomicAdd(a.unit_counter, 1u);
+        c = (a.unit_order != nullptr && k < n_units) ? static_cast<int64_t>(a.unit_order[k])
+                                                     : static_cast<int64_t>(k);
+      } else {
+        c = blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
+      }
+    }
+    return c;   // lane 0's value counts
+  };
+  int64_t u_next = claim(0);
   for (uint32_t U = 0;; ++U) {
     const int sl = static_cast<int>(U % kRing);
     unsigned char* slot = smem + P.ring + sl * P.slot_bytes;
@@ -380,21 +423,7 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
       if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
-    // The next unit: claimed from the forward's counter (whichever CTA is
-    // free takes the next unit in index order, so heavy units of a skewed
-    // selection do not pile up on a few CTAs), or round-robin without one.
-    // With a longest-first list the counter walks that list instead.
-    int64_t u = 0;
-    if (lane == 0) {
-      if (a.unit_counter != nullptr) {
-        const uint32_t k = atomicAdd(a.unit_counter, 1u);
-        u = (a.unit_order != nullptr && k < n_units) ? static_cast<int64_t>(a.unit_order[k])
-                                                     : static_cast<int64_t>(k);
-      } else {
-        u = blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
-      }
-    }
-    u = __shfl_sync(kAll, u, 0);
+    const int64_t u = __shfl_sync(kAll, u_next, 0);
     if (u >= n_units) {
       // end of work: a unit with rows < 0 tells the other roles to stop
       if (lane == 0) reinterpret_cast<UnitInfo*>(slot)->rows = -1;
@@ -408,6 +437,7 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     else if (lane == 1) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j];
     else if (lane == 2) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j + 1];
     else if (lane == 3) x = a.edge_head_base[h];
+    u_next = claim(U + 1);
     const int raw = static_cast<int>(__shfl_sync(kAll, x, 0));
     const int64_t ebase = __shfl_sync(kAll, x, 3);
     const int64_t e0 = ebase + __shfl_sync(kAll, x, 1);
@@ -416,31 +446,43 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     if (bad && lane == 0) report(status, SA_ERR_SHAPE);
     const int b = bad ? 0 : raw / a.msb;
     const int blk = bad ? 0 : raw - b * a.msb;
+    // One round trip for the rest: the sequence's lengths, the block's page
+    // ids and the first tile's query ids are all issued before any is used.
     int64_t y = 0;
     if (lane == 0) y = a.used ? max(a.used[b], 0) : static_cast<int64_t>(a.msb) * BS;
     else if (lane == 1) y = a.cu[b];
     else if (lane == 2) y = a.cu[b + 1];
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
+                        static_cast<int64_t>(blk) * a.pages_per_block;
+    int pid[BS / 32];
+#pragma unroll
+    for (int q = 0; q < BS / 32; ++q) pid[q] = bad ? -1 : bt[(lane + 32 * q) / ps];
+    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
+    int64_t qi[kM / 32];
+#pragma unroll
+    for (int q = 0; q < kM / 32; ++q) {
+      const int r = lane + 32 * q;
+      qi[q] = r < rows ? a.edges[2 * (e0 + r / qhead)] : -1;
+    }
     const int64_t lk = __shfl_sync(kAll, y, 0);
     const int64_t q0 = __shfl_sync(kAll, y, 1);
     const int64_t qo = __shfl_sync(kAll, y, 2) - q0;
-    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
     const int64_t bstart = static_cast<int64_t>(blk) * BS;
     const int64_t bend = min(bstart + BS, lk);
     // the keys: position (or -1) and source offset through the block table
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
-                        static_cast<int64_t>(blk) * a.pages_per_block;
     int64_t* koff = reinterpret_cast<int64_t*>(slot + L::koff);
     int32_t* kpos = reinterpret_cast<int32_t*>(slot + L::kpos);
-    for (int jj = lane; jj < BS; jj += 32) {
+#pragma unroll
+    for (int q = 0; q < BS / 32; ++q) {
+      const int jj = lane + 32 * q;
       const int64_t pos = bstart + jj;
       int32_t live = -1;
       int64_t off = -1;
       if (!bad && pos < bend) {
-        const int pid = bt[jj / ps];
-        if (pid >= a.num_pages) report(status, SA_ERR_SHAPE);
-        if (pid >= 0 && pid < a.num_pages) {
+        if (pid[q] >= a.num_pages) report(status, SA_ERR_SHAPE);
+        if (pid[q] >= 0 && pid[q] < a.num_pages) {
           live = static_cast<int32_t>(pos);
-          off = ((static_cast<int64_t>(pid) * a.hkv + h) * ps + jj % ps) * kD;
+          off = ((static_cast<int64_t>(pid[q]) * a.hkv + h) * ps + jj % ps) * kD;
         }
       }
       kpos[jj] = live;
@@ -448,13 +490,11 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     }
     // the first tile's Q sources
     int64_t* qsrc = reinterpret_cast<int64_t*>(slot + L::qsrc);
-    for (int r = lane; r < kM; r += 32) {
-      int64_t src = -1;
-      if (r < rows) {
-        const int64_t qi = a.edges[2 * (e0 + r / qhead)];
-        src = (qi * a.hq + static_cast<int64_t>(h) * qhead + r % qhead) * kD;
-      }
-      qsrc[r] = src;
+#pragma unroll
+    for (int q = 0; q < kM / 32; ++q) {
+      const int r = lane + 32 * q;
+      qsrc[r] = qi[q] >= 0 ? (qi[q] * a.hq + static_cast<int64_t>(h) * qhead + r % qhead) * kD
+                           : int64_t{-1};
     }
     if (lane == 0 && a.cta_stats != nullptr && static_cast<int>(blockIdx.x) < a.cta_stats_len) {
       unsigned long long* st = reinterpret_cast<unsigned long long*>(a.cta_stats) + 3 * blockIdx.x;
@@ -520,17 +560,17 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
     const int64_t* koff = reinterpret_cast<const int64_t*>(slot + L::koff);
     const int32_t* skpos = reinterpret_cast<const int32_t*>(slot + L::kpos);
     for (int jj = lt; jj < BS; jj += kLoadThreads) kpos[jj] = skpos[jj];
-    // K and V rows alike (lane = 4 dims, converted to bf16 unless the
-    // operands stay f32), ten of a warp's rows in flight at a time: rows
-    // [0, BS) are K, [BS, 2 BS) V, both stored [key][128] with the 128-byte
-    // swizzle (V is the MMA's MN-major B operand).
+    // K and V rows alike (lane = 4 dims, converted to bf16, except K rows
+    // kept f32 for tf32 scores), 13 of a warp's rows in flight at a time:
+    // rows [0, BS) are K, [BS, 2 BS) V, both stored [key][128] with the
+    // 128-byte swizzle (V is the MMA's MN-major B operand).
     if constexpr (kTf32) {
       constexpr int kRows = (2 * BS + kLoaders - 1) / kLoaders;
 #pragma unroll
-      for (int q0 = 0; q0 < kRows; q0 += 10) {
-        float4 kr[10];
+      for (int q0 = 0; q0 < kRows; q0 += kKvBatch) {
+        float4 kr[kKvBatch];
 #pragma unroll
-        for (int q = 0; q < 10; ++q) {
+        for (int q = 0; q < kKvBatch; ++q) {
           const int r = lw + (q0 + q) * kLoaders;
           const int key = r < BS ? r : r - BS;
           const int64_t off = q0 + q < kRows && r < 2 * BS ? koff[key] : -1;
@@ -540,22 +580,24 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int q = 0; q < 10; ++q) {
+        for (int q = 0; q < kKvBatch; ++q) {
           const int r = lw + (q0 + q) * kLoaders;
           if (q0 + q < kRows && r < 2 * BS) {
-            const int key = r < BS ? r : r - BS;
-            *reinterpret_cast<float4*>((r < BS ? ks : vs) + sw128_offset_f32(BS, key, 4 * lane)) =
-                kr[q];
+            if (r < BS)       // K: f32 rows (tf32 operand)
+              *reinterpret_cast<float4*>(ks + sw128_offset_f32(BS, r, 4 * lane)) = kr[q];
+            else              // V: bf16 rows (bf16 operand of O = P V)
+              *reinterpret_cast<uint2*>(vs + sw128_offset(BS, r - BS, 4 * lane)) =
+                  make_uint2(pack_bf16x2_rn(kr[q].x, kr[q].y), pack_bf16x2_rn(kr[q].z, kr[q].w));
           }
         }
       }
     } else {
       constexpr int kRows = (2 * BS + kLoaders - 1) / kLoaders;
 #pragma unroll
-      for (int q0 = 0; q0 < kRows; q0 += 10) {
-        uint2 kr[10];
+      for (int q0 = 0; q0 < kRows; q0 += kKvBatch) {
+        uint2 kr[kKvBatch];
 #pragma unroll
-        for (int q = 0; q < 10; ++q) {
+        for (int q = 0; q < kKvBatch; ++q) {
           const int r = lw + (q0 + q) * kLoaders;
           const int key = r < BS ? r : r - BS;
           const int64_t off = q0 + q < kRows && r < 2 * BS ? koff[key] : -1;
@@ -563,7 +605,7 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
                            : make_uint2(0u, 0u);
         }
 #pragma unroll
-        for (int q = 0; q < 10; ++q) {
+        for (int q = 0; q < kKvBatch; ++q) {
           const int r = lw + (q0 + q) * kLoaders;
           if (q0 + q < kRows && r < 2 * BS) {
             const int key = r < BS ? r : r - BS;
@@ -691,19 +733,13 @@ __device__ bool tc_issue_o(unsigned char* smem, const TcPlan& P, const TcBars& B
   tc_fence_after();
   constexpr int E = TcCfg<BS, kTf32>::E;
   const uint32_t v_addr = smem_u32(smem + P.kv + kvb * P.kv_bytes + static_cast<size_t>(BS) * kD * E);
-  const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs, or f32) over S's columns
+  const uint32_t t_p = tmem + 128 * sb;          // P (bf16 pairs) over S's columns
   const uint32_t t_o = tmem + 256 + 128 * sb;
-  if constexpr (kTf32) {
+  // P of keys 0..63 in columns 0..31, of keys 64..127 in columns 64..95
 #pragma unroll
-    for (int st = 0; st < BS / 8; ++st)  // 8 keys = 1024 bytes of V rows per step
-      mma_tf32_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 1024, BS * 128),
-                  idesc_tf32(kM, kD, true), st > 0);
-  } else {
-#pragma unroll
-    for (int st = 0; st < BS / 16; ++st)  // 16 keys = 2048 bytes of V rows per step
-      mma_bf16_ta(t_o, t_p + 8 * st, sw128_desc_mn(v_addr + st * 2048, BS * 128),
-                  idesc_bf16(kM, kD, true), st > 0);
-  }
+  for (int st = 0; st < BS / 16; ++st)   // 16 keys = 2048 bytes of V rows per step
+    mma_bf16_ta(t_o, t_p + 8 * st + (st >= 4 ? 32 : 0),
+                sw128_desc_mn(v_addr + st * 2048, BS * 128), idesc_bf16(kM, kD, true), st > 0);
   mma_commit(B.o_full + sb);
   mma_commit(B.s_free + sb);                     // P read: the S / P columns are free
   return true;
@@ -819,7 +855,7 @@ template <int BS, bool kTf32>
 __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsigned char* smem,
                            const TcPlan& P, const TcBars& B, uint32_t tmem, int warp,
                            int lane) {
-  const uint32_t g = static_cast<uint32_t>((warp - 1 - kLoaders) >> 2);
+  const uint32_t g = static_cast<uint32_t>((warp - kSoftmaxWarp0) >> 2);
   constexpr int KVB = TcCfg<BS, kTf32>::KVB;
   int64_t* status = a.totals + 3;
   const int row = (warp & 3) * 32 + lane;               // TMEM lane = tile row
@@ -878,6 +914,8 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         bulk_commit();
       }
     };
+    // O 32 columns at a time (the epilogue keeps the softmax loop's state
+    // live, so a 64-column load would spill)
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       float v[32];
@@ -991,87 +1029,95 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
       }
       tc_fence_after();
       const uint32_t t_s = tmem + 128 * sb + lane_base;
-      // pass 1: the row maximum of qscale * s over live keys, as qscale
-      // times the largest (qscale >= 0) or smallest raw score: rounding is
-      // monotonic, so the product is the same maximum (fully live chunks, the
-      // common case, without per-key masks, three scores per instruction)
+      // S in halves of 64 keys, each read with one TMEM load (one round trip):
+      // pass 1 takes the row maximum of qscale * s over live keys, as qscale
+      // times the largest (qscale >= 0) or smallest raw score (rounding is
+      // monotonic, so the product is the same maximum; fully live chunks, the
+      // common case, without per-key masks, three scores per instruction).
+      // Pass 2 turns each half into p = exp(s - m), l, and P as bf16 pairs
+      // (16 columns per 32 keys): the half pass 1 read last is still in
+      // registers and goes first, its P into columns 64.. of S (already
+      // read), then the first half's P into columns 0..; the P V MMA reads
+      // keys 64.. from there.
+      constexpr int NH = BS / 64;
+      auto live_of = [&](int c) -> uint32_t {      // live keys of 32-key chunk c
+        const int cut = jlim - c * 32;
+        const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
+        return vmask[c] & inside;
+      };
       const bool up = qscale >= 0.f;
       float ext = up ? -INFINITY : INFINITY;
       bool any = false;
-#pragma unroll 1
-      for (int c = 0; c < BS / 32; ++c) {
-        float v[32];
-        tmem_ld32(t_s + c * 32, v);
+      float v[64];
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        tmem_ld64(t_s + hh * 64, v);
         tmem_ld_wait();
-        const int cut = jlim - c * 32;
-        const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
-        const uint32_t live = vmask[c] & inside;
-        any = any || live != 0u;
-        if (live == 0xffffffffu) {
-          if (up) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) ext = max3(ext, v[i], v[i + 1]);
-          } else {
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const uint32_t live = live_of(2 * hh + c2);
+          const float* x = v + 32 * c2;
+          any = any || live != 0u;
+          if (live == 0xffffffffu) {
+            if (up) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) ext = min3(ext, v[i], v[i + 1]);
+              for (int i = 0; i < 32; i += 2) ext = max3(ext, x[i], x[i + 1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) ext = min3(ext, x[i], x[i + 1]);
+            }
+          } else if (live) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if ((live >> i) & 1u) ext = up ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
           }
-        } else if (live) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((live >> i) & 1u) ext = up ? fmaxf(ext, v[i]) : fminf(ext, v[i]);
         }
       }
       const float m2 = any ? ext * qscale : -INFINITY;
-      // pass 2: p = exp(s - m), l, and P into the S columns already read:
-      // bf16 pairs (chunk c's 16 columns lie at or before S chunk c), or, for
-      // tf32 operands, f32 in place of S chunk c.
       const float msub = m2 == -INFINITY ? 0.f : m2;
       const uint64_t qs2 = f32x2(qscale, qscale);
       const uint64_t nm2 = f32x2(-msub, -msub);
       uint64_t l2 = f32x2(0.f, 0.f);          // two partial sums of p
-#pragma unroll 1
-      for (int c = 0; c < BS / 32; ++c) {
-        float v[32];
-        tmem_ld32(t_s + c * 32, v);
-        tmem_ld_wait();
-        const int cut = jlim - c * 32;
-        const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
-        const uint32_t live = vmask[c] & inside;
-        uint32_t pk[kTf32 ? 32 : 16];
-        auto put = [&](int i2, float p0, float p1) {
-          if constexpr (kTf32) {
-            pk[2 * i2] = __float_as_uint(p0);
-            pk[2 * i2 + 1] = __float_as_uint(p1);
+      // P of half hh (v) into pk[32]
+      auto p_half = [&](int hh, uint32_t (&pk)[32]) {
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const uint32_t live = live_of(2 * hh + c2);
+          const float* x = v + 32 * c2;
+          if (live == 0xffffffffu) {
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+              float x0, x1;
+              f32x2_split(fma_f32x2(f32x2(x[2 * i2], x[2 * i2 + 1]), qs2, nm2), x0, x1);
+              const float p0 = ex2_fast(x0);
+              const float p1 = ex2_fast(x1);
+              l2 = add_f32x2(l2, f32x2(p0, p1));
+              pk[16 * c2 + i2] = pack_bf16x2_rn(p0, p1);
+            }
           } else {
-            pk[i2] = pack_bf16x2_rn(p0, p1);
-          }
-        };
-        if (live == 0xffffffffu) {
 #pragma unroll
-          for (int i2 = 0; i2 < 16; ++i2) {
-            float x0, x1;
-            f32x2_split(fma_f32x2(f32x2(v[2 * i2], v[2 * i2 + 1]), qs2, nm2), x0, x1);
-            const float p0 = ex2_fast(x0);
-            const float p1 = ex2_fast(x1);
-            l2 = add_f32x2(l2, f32x2(p0, p1));
-            put(i2, p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int i2 = 0; i2 < 16; ++i2) {
-            const int i = 2 * i2;
-            float x0, x1;
-            f32x2_split(fma_f32x2(f32x2(v[i], v[i + 1]), qs2, nm2), x0, x1);
-            const float p0 = ((live >> i) & 1u) ? ex2_fast(x0) : 0.f;
-            const float p1 = ((live >> (i + 1)) & 1u) ? ex2_fast(x1) : 0.f;
-            l2 = add_f32x2(l2, f32x2(p0, p1));
-            put(i2, p0, p1);
+            for (int i2 = 0; i2 < 16; ++i2) {
+              const int i = 2 * i2;
+              float x0, x1;
+              f32x2_split(fma_f32x2(f32x2(x[i], x[i + 1]), qs2, nm2), x0, x1);
+              const float p0 = ((live >> i) & 1u) ? ex2_fast(x0) : 0.f;
+              const float p1 = ((live >> (i + 1)) & 1u) ? ex2_fast(x1) : 0.f;
+              l2 = add_f32x2(l2, f32x2(p0, p1));
+              pk[16 * c2 + i2] = pack_bf16x2_rn(p0, p1);
+            }
           }
         }
-        if constexpr (kTf32)
-          tmem_st32(t_s + c * 32, pk);
-        else
-          tmem_st16(t_s + c * 16, pk);
+      };
+      {
+        uint32_t pk[32];
+        if constexpr (NH == 2) {
+          p_half(1, pk);                     // keys 64..127, still in registers
+          tmem_st32(t_s + 64, pk);           // over S columns already read
+          tmem_ld64(t_s, v);                 // keys 0..63
+          tmem_ld_wait();
+        }
+        p_half(0, pk);
+        tmem_st32(t_s, pk);
       }
       float la, lb;
       f32x2_split(l2, la, lb);
@@ -1170,23 +1216,24 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int64_t n_units = unit_base[a.hkv];
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tc_mma<BS, kTf32>(a, smem, P, B, tmem);
-      // Every MMA issued has completed before TMEM is released.
-      mma_commit(B.done);
-      if (!mbar_wait_bounded(B.done, 0)) report(a.totals + 3, SA_ERR_DEVICE_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp <= kLoaders) {
-    tc_loader<BS, kBf16, kTf32>(a, smem, P, B, warp - 1, lane);
-  } else if (warp < kSchedWarp) {
+  if (warp >= kSoftmaxWarp0) {
     tc_softmax<BS, kTf32>(a, &omap, smem, P, B, tmem, warp, lane);
     // box stores issued by this thread have landed before the CTA leaves
     bulk_wait_all();
   } else {
-    tc_scheduler<BS>(a, smem, P, B, unit_base, n_units, lane);
+    if (warp == 0) {
+      if (lane == 0) {
+        tc_mma<BS, kTf32>(a, smem, P, B, tmem);
+        // Every MMA issued has completed before TMEM is released.
+        mma_commit(B.done);
+        if (!mbar_wait_bounded(B.done, 0)) report(a.totals + 3, SA_ERR_DEVICE_TIMEOUT);
+      }
+      __syncwarp();
+    } else if (warp == kSchedWarp) {
+      tc_scheduler<BS>(a, smem, P, B, unit_base, n_units, lane);
+    } else {
+      tc_loader<BS, kBf16, kTf32>(a, smem, P, B, warp - kLoaderWarp0, lane);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1197,20 +1244,23 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
 }
 
 // The longest-first work list: every unit (kv head, compact slot) of the
-// index, numbered across heads as the scheduler numbers them, sorted by
-// descending edge count (a counting sort over kOrderBins counts; counts
-// above the last bin share it; equal counts in no particular order, which
-// changes which CTA runs a unit but no result).  One CTA: the list is a
-// few tens of thousands of entries at most.
+// index, numbered across heads as the scheduler numbers them, in classes of
+// descending size (class c: 2^c <= edges < 2^(c+1), the last class open),
+// largest class first.  Inside a class each warp places its 32 consecutive
+// units together, in index order, with one atomic per warp and class, so
+// runs of neighbouring blocks (which share their queries' Q rows in L2) stay
+// together; which run comes first is not fixed, which changes which CTA runs
+// a unit but no result.  One CTA: the list is a few tens of thousands of
+// entries at most.
 constexpr int kOrderThreads = 1024;
-constexpr int kOrderBins = 2048;
+constexpr int kOrderClasses = 16;
 constexpr int kOrderBatch = 8;     // units whose counts are in flight per thread
 
 __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a) {
   __shared__ int32_t ubase[201];
-  __shared__ uint32_t bins[kOrderBins];
-  __shared__ uint32_t warp_tot[kOrderThreads / 32];
+  __shared__ uint32_t cursor[kOrderClasses];
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
   if (tid == 0) {
     int32_t acc = 0;
     for (int hh = 0; hh < a.hkv; ++hh) {
@@ -1219,11 +1269,11 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a
     }
     ubase[a.hkv] = acc > a.max_units ? static_cast<int32_t>(a.max_units) : acc;
   }
-  for (int b = tid; b < kOrderBins; b += kOrderThreads) bins[b] = 0;
+  if (tid < kOrderClasses) cursor[tid] = 0;
   __syncthreads();
   const int64_t n = ubase[a.hkv];
-  // bin of unit u: kOrderBins - 1 - min(edges, kOrderBins - 1) (most edges first)
-  auto bins_of = [&](int64_t u0, int (&bin)[kOrderBatch]) {
+  // class of unit u, -1 past the end: floor(log2(edges)), at most the last
+  auto classes_of = [&](int64_t u0, int (&cls)[kOrderBatch]) {
     int32_t lo[kOrderBatch], hi[kOrderBatch];
 #pragma unroll
     for (int q = 0; q < kOrderBatch; ++q) {
@@ -1239,53 +1289,49 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a
     }
 #pragma unroll
     for (int q = 0; q < kOrderBatch; ++q) {
-      int c = hi[q] - lo[q];
-      c = c < 0 ? 0 : (c > kOrderBins - 1 ? kOrderBins - 1 : c);
-      bin[q] = kOrderBins - 1 - c;
+      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
+      const int c = max(hi[q] - lo[q], 1);
+      cls[q] = u < n ? min(31 - __clz(c), kOrderClasses - 1) : -1;
     }
   };
   const int64_t step = static_cast<int64_t>(kOrderThreads) * kOrderBatch;
-  for (int64_t u0 = tid; u0 < n; u0 += step) {
-    int bin[kOrderBatch];
-    bins_of(u0, bin);
-#pragma unroll
-    for (int q = 0; q < kOrderBatch; ++q)
-      if (u0 + static_cast<int64_t>(q) * kOrderThreads < n) atomicAdd(&bins[bin[q]], 1u);
-  }
-  __syncthreads();
-  // exclusive scan of the bins: two per thread, then across the warps
-  constexpr int kPer = kOrderBins / kOrderThreads;
-  uint32_t v[kPer], sum = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    v[i] = bins[tid * kPer + i];
-    sum += v[i];
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t inc = sum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += x;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  uint32_t before = 0;
-  for (int w = 0; w < warp; ++w) before += warp_tot[w];
-  uint32_t run = before + inc - sum;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    bins[tid * kPer + i] = run;
-    run += v[i];
-  }
-  __syncthreads();
-  for (int64_t u0 = tid; u0 < n; u0 += step) {
-    int bin[kOrderBatch];
-    bins_of(u0, bin);
+  // pass 1: class sizes (one shared-memory atomic per warp and class
+  // present); their exclusive prefix, largest class first
+  for (int64_t u0 = tid - lane; u0 < n; u0 += step) {
+    int cls[kOrderBatch];
+    classes_of(u0 + lane, cls);
 #pragma unroll
     for (int q = 0; q < kOrderBatch; ++q) {
-      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
-      if (u < n) a.unit_order[atomicAdd(&bins[bin[q]], 1u)] = static_cast<int32_t>(u);
+      const unsigned peers = __match_any_sync(0xffffffffu, cls[q]);
+      if (cls[q] >= 0 && lane == __ffs(peers) - 1)
+        atomicAdd(&cursor[cls[q]], static_cast<uint32_t>(__popc(peers)));
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t run = 0;
+    for (int c = kOrderClasses - 1; c >= 0; --c) {
+      const uint32_t x = cursor[c];
+      cursor[c] = run;
+      run += x;
+    }
+  }
+  __syncthreads();
+  // pass 2: each warp's runs of 32 consecutive units, class by class
+  for (int64_t u0 = tid - lane; u0 < n; u0 += step) {
+    int cls[kOrderBatch];
+    classes_of(u0 + lane, cls);
+#pragma unroll
+    for (int q = 0; q < kOrderBatch; ++q) {
+      const int64_t u = u0 + lane + static_cast<int64_t>(q) * kOrderThreads;
+      const unsigned peers = __match_any_sync(0xffffffffu, cls[q]);
+      const int leader = __ffs(peers) - 1;
+      uint32_t base = 0;
+      if (cls[q] >= 0 && lane == leader)
+        base = atomicAdd(&cursor[cls[q]], static_cast<uint32_t>(__popc(peers)));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (cls[q] >= 0)
+        a.unit_order[base + __popc(peers & ((1u << lane) - 1u))] = static_cast<int32_t>(u);
     }
   }
 }

@@ -171,6 +171,57 @@ __device__ __forceinline__ void locate(int64_t c, const int32_t* chunk_base, int
   k = r - chunk_base[lo];
 }
 
+// ---- warp-per-segment mode (every segment holds at most 64 entries) --------
+// Entry t of segment (h, b) (query cu[b] + t / topk, rank t % topk) sits in
+// lane t & 31 of round t >> 5.  With 64 entries at most, every statistic of
+// the counting sort comes from one pass of warp shuffles over the entries:
+// for entry t with block x (kept entries only),
+//   same   kept entries with block x,
+//   before kept entries with block x and a smaller t (0: t opens its bucket),
+//   less   kept entries with a smaller block.
+struct SmallSeg {
+  int blk[2];        // block of the entry, -1 when dropped
+  int same[2], before[2], less[2];
+};
+
+__device__ __forceinline__ void small_segment(const IndexArgs& a, int h, int b, int lane,
+                                              bool check, int64_t* status, SmallSeg& g,
+                                              int& n_out) {
+  const int64_t q0 = a.cu[b];
+  const int n = static_cast<int>((a.cu[b + 1] - q0) * a.topk);
+  const int64_t lk = a.used ? (a.used[b] > 0 ? a.used[b] : 0)
+                            : static_cast<int64_t>(a.msb) * a.block_size;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int t = 32 * k + lane;
+    g.blk[k] = -1;
+    if (t < n) {
+      const int64_t i = q0 + t / a.topk;
+      const int r = t % a.topk;
+      const int x = a.selected[(i * a.hkv + h) * a.topk + r];
+      if (check && (x < -1 || x >= a.msb)) report(status, SA_ERR_SELECTED_RANGE);
+      if (x >= 0 && x < a.msb && static_cast<int64_t>(x) * a.block_size < lk) g.blk[k] = x;
+    }
+    g.same[k] = g.before[k] = g.less[k] = 0;
+  }
+  for (int j = 0; j < n; ++j) {
+    const int xj = __shfl_sync(0xffffffffu, j < 32 ? g.blk[0] : g.blk[1], j & 31);
+    if (xj < 0) continue;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int t = 32 * k + lane;
+      if (g.blk[k] < 0) continue;
+      if (xj == g.blk[k]) {
+        ++g.same[k];
+        if (j < t) ++g.before[k];
+      } else if (xj < g.blk[k]) {
+        ++g.less[k];
+      }
+    }
+  }
+  n_out = n;
+}
+
 __global__ void __launch_bounds__(kThreads, 4)
 index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   extern __shared__ int64_t dyn64[];
@@ -204,7 +255,7 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   // chunk_base[b]: chunks of the sequences before b; multi_base[b]: the same
   // over sequences of several chunks.  One block scan per kThreads sequences
   // (the cu reads of a tile are issued together, not one after another).
-  {
+  if (!a.small) {
     int64_t carry_c = 0, carry_m = 0;
     for (int base = 0; base < batch; base += kThreads) {
       const int b = base + tid;
@@ -244,7 +295,36 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   const int nmulti = s.nmulti_head;
 
   // ---- phase 1: per-chunk histograms and segment totals ---------------------
-  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+  if (a.small) {
+    // one warp per segment (segments spread over the CTAs first, then over
+    // their warps): kept entries, distinct blocks, work splits
+    for (int seg = warp * gridDim.x + blockIdx.x; seg < nseg; seg += gridDim.x * kWarps) {
+      const int h = seg / batch, b = seg - (seg / batch) * batch;
+      SmallSeg g;
+      int n = 0;
+      small_segment(a, h, b, lane, false, status, g, n);
+      int64_t v[3] = {0, 0, 0};
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (g.blk[k] >= 0) {
+          v[0] += 1;
+          if (g.before[k] == 0) {
+            v[1] += 1;
+            v[2] += splits_of(g.same[k], a.split_edges);
+          }
+        }
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+      if (lane == 0) {
+        seg_tot[3 * seg + 0] = static_cast<int32_t>(v[0]);
+        seg_tot[3 * seg + 1] = static_cast<int32_t>(v[1]);
+        seg_tot[3 * seg + 2] = static_cast<int32_t>(v[2]);
+      }
+    }
+  }
+  for (int64_t c = a.small ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
     int h, b, k;
     locate(c, chunk_base, batch, nch_head, h, b, k);
     const int nc = chunk_base[b + 1] - chunk_base[b];
@@ -304,7 +384,7 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
     __syncthreads();
   }
   // Segments without entries have no chunk: their totals are zero.
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < nseg;
+  for (int64_t g = a.small ? nseg : static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < nseg;
        g += static_cast<int64_t>(gridDim.x) * kThreads) {
     const int b = static_cast<int>(g % batch);
     if (chunk_base[b + 1] == chunk_base[b]) {
@@ -353,7 +433,84 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   __syncthreads();
 
   // ---- phase 2: prefixes, slot writes, stable scatter ----------------------
-  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+  if (a.small) {
+    // one warp per segment: entry t goes to edge pre + less + before (blocks
+    // ascending, (query, rank) ascending inside a block); the entry that
+    // opens a bucket writes its compact slot and its work splits, placed by
+    // the buckets of smaller blocks (ranks among the opening entries)
+    for (int seg = warp * gridDim.x + blockIdx.x; seg < nseg; seg += gridDim.x * kWarps) {
+      const int h = seg / batch, b = seg - (seg / batch) * batch;
+      SmallSeg g;
+      int n = 0;
+      small_segment(a, h, b, lane, true, status, g, n);
+      int64_t pre[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) pre[j] = *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * seg + j);
+      const int64_t head_edges =
+          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 0);
+      const int64_t head_units =
+          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 1);
+      // ranks among the opening entries: units and splits of smaller blocks
+      int ul[2] = {0, 0};
+      int64_t sl[2] = {0, 0};
+      for (int j = 0; j < n; ++j) {
+        const int src = j & 31;
+        const bool lo = j < 32;
+        const int xj = __shfl_sync(0xffffffffu, lo ? g.blk[0] : g.blk[1], src);
+        const int bj = __shfl_sync(0xffffffffu, lo ? g.before[0] : g.before[1], src);
+        const int sj = __shfl_sync(0xffffffffu, lo ? g.same[0] : g.same[1], src);
+        if (xj < 0 || bj != 0) continue;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (g.blk[k] >= 0 && xj < g.blk[k]) {
+            ++ul[k];
+            sl[k] += splits_of(sj, a.split_edges);
+          }
+      }
+      const int64_t q0 = a.cu[b];
+      const int64_t nbs = a.nbs;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int t = 32 * k + lane;
+        if (t >= n) continue;
+        const int64_t i = q0 + t / topk;
+        const int r = t % topk;
+        const int64_t inv_at = (static_cast<int64_t>(h) * a.tq + i) * topk + r;
+        if (g.blk[k] < 0) {
+          a.idx.inv[inv_at] = -1;
+          continue;
+        }
+        const int64_t first = pre[0] + g.less[k];          // absolute edge of the bucket
+        const int64_t pos = first + g.before[k];
+        if (pos >= 0 && pos < cap) {
+          reinterpret_cast<int2*>(a.idx.edges)[pos] = make_int2(static_cast<int32_t>(i), r);
+          a.idx.inv[inv_at] = static_cast<int32_t>(pos - head_edges);
+        }
+        if (g.before[k] != 0) continue;
+        const int64_t j = pre[1] - head_units + ul[k];
+        if (j >= 0 && j < nbs) {
+          a.idx.sel_slots[h * nbs + j] = static_cast<int32_t>(static_cast<int64_t>(b) * msb + g.blk[k]);
+          a.idx.sel_offsets[h * (nbs + 1) + j] = static_cast<int32_t>(first - head_edges);
+        }
+        const int cnt = g.same[k];
+        const int step = a.split_edges > 0 ? a.split_edges : cnt;
+        const int64_t nsp = splits_of(cnt, a.split_edges);
+        for (int64_t u = 0; u < nsp; ++u) {
+          const int64_t gs = pre[2] + sl[k] + u;
+          if (gs < cap) {
+            const int64_t lo_e = first + u * step;
+            int4 w;
+            w.x = h;
+            w.y = static_cast<int32_t>(j);
+            w.z = static_cast<int32_t>(lo_e);
+            w.w = static_cast<int32_t>(min(lo_e + step, first + cnt));
+            reinterpret_cast<int4*>(a.idx.splits)[gs] = w;
+          }
+        }
+      }
+    }
+  }
+  for (int64_t c = a.small ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
     int h, b, k;
     locate(c, chunk_base, batch, nch_head, h, b, k);
     const int nc = chunk_base[b + 1] - chunk_base[b];
@@ -605,14 +762,17 @@ cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
   const int64_t n_chunks = chunks_per_head * a.hkv;
   int64_t grid = static_cast<int64_t>(per_sm) * device_sm_count();
   const int64_t plateau_ctas = (static_cast<int64_t>(a.hkv) * (a.nbs + 1) + kThreads - 1) / kThreads;
-  const int64_t want = std::max<int64_t>(std::max<int64_t>(n_chunks, plateau_ctas), 1);
+  // work items: chunks, or in warp-per-segment mode warps' worth of segments
+  const int64_t items =
+      a.small ? (static_cast<int64_t>(a.hkv) * a.batch + kWarps - 1) / kWarps : n_chunks;
+  const int64_t want = std::max<int64_t>(std::max<int64_t>(items, plateau_ctas), 1);
   if (grid > want) grid = want;
   IndexArgs args = a;
   int site = kStallNone;
   debug_stall_setting(&site, &args.spin_limit);
   args.stall = site == kStallIndexBarrier;
   WorkspaceLayout layout = lay;
-  int64_t nch = n_chunks;
+  int64_t nch = a.small ? 0 : n_chunks;
   void* params[] = {&args, &layout, &nch};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(index_kernel),
                                      dim3(static_cast<unsigned>(grid)), dim3(kThreads), params,

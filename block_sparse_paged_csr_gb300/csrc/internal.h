@@ -64,7 +64,13 @@ struct IndexArgs {
   sa_index idx;             // output arrays + workspace
   uint32_t spin_limit;      // tries of the grid barrier's wait (0 = kSpinLimit)
   int stall;                // test hook: the grid barrier is never released
+  int small;                // every segment holds at most kSmallSegment entries
+                            // (decode batches): one warp per segment
 };
+
+// Largest segment (entries of one (kv head, sequence)) of the index kernel's
+// warp-per-segment mode: two entries per lane.
+constexpr int kSmallSegment = 64;
 
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
                                int64_t hist_slots_per_head, cudaStream_t stream);

@@ -71,9 +71,7 @@ typedef enum sa_path {
                                     problems with bf16 K/V use warp-level MMA (Q and
                                     P split into two bf16 parts); others use the
                                     tcgen05 kernel (block 64 or 128, qhead dividing
-                                    128): bf16 operands for bf16 K/V, tf32 operands
-                                    (Q, K, V and P kept in f32 in shared and tensor
-                                    memory) for f32 K/V; f32 accumulation;
+                                    128, bf16 operands); f32 accumulation;
                                     SA_ERR_UNSUPPORTED elsewhere                   */
   SA_PATH_CUDA_CORE_GENERAL = 3, /* the general f32 FMA kernel only                 */
   SA_PATH_FUSED_DECODE = 4,      /* sa_attention / sa_forward_combine only: forward
@@ -81,9 +79,12 @@ typedef enum sa_path {
                                     holds at most one query (see sa_attention);
                                     SA_ERR_UNSUPPORTED elsewhere and from
                                     sa_forward                                   */
-  SA_PATH_TENSOR_CORE_BF16 = 5   /* as SA_PATH_TENSOR_CORE, but the tcgen05 kernel
-                                    rounds f32 K/V, Q and P to bf16 operands too
-                                    (half the shared-memory bytes of tf32; looser) */
+  SA_PATH_TENSOR_CORE_TF32 = 5   /* as SA_PATH_TENSOR_CORE, but with f32 K/V the
+                                    tcgen05 kernel forms the scores S = Q K^T from
+                                    Q and K kept in f32 (tf32 operands) and only
+                                    P and V are rounded to bf16: about half the
+                                    error of bf16 operands, at the cost of twice
+                                    the shared-memory bytes of Q and K          */
 } sa_path;
 
 /*
@@ -271,9 +272,9 @@ sa_status sa_build_index_no_alloc(const int32_t *selected, int64_t tq, int32_t h
  * SA_ERR_UNSUPPORTED.  SA_PATH_AUTO sends decode-shaped problems (tq at most
  * twice the batch) to the pipelined CUDA-core kernel (f32 K/V) or to the
  * warp-level MMA kernel (bf16 K/V), and the others to the tcgen05 kernel
- * where supported (tf32 operands for f32 K/V, bf16 for bf16 K/V; use
- * SA_PATH_CUDA_CORE for f32 arithmetic throughout, SA_PATH_TENSOR_CORE_BF16
- * for bf16 operands with f32 K/V).  The tcgen05 kernel claims work units from a
+ * where supported (operands rounded to bf16; use SA_PATH_TENSOR_CORE_TF32 for
+ * tf32 scores with f32 K/V, SA_PATH_CUDA_CORE for f32 arithmetic
+ * throughout).  The tcgen05 kernel claims work units from a
  * counter in the first 256 bytes of the index's scratch (cleared on the
  * stream before each launch): idx->workspace when it is set and
  * idx->workspace_bytes is at least 256, the library's array for an index

@@ -252,7 +252,7 @@ def _check_hot_units(w, ih, parts, n_units, tol, name):
 # --------------------------------------------------------------------------- each kernel
 
 
-def _check_against_oracle(w, t, split, path, tol=_gpu.TOL_F32):
+def _check_against_oracle(w, t, split, path, tol=_gpu.TOL_F32, report=None):
     out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=split, path=path)
     ref_out, ref_lse, ref_idx, (ro, rm, rl) = _oracle_attention(w, split)
     _gpu.compare_index(idx.to_host(), ref_idx)
@@ -261,6 +261,9 @@ def _check_against_oracle(w, t, split, path, tol=_gpu.TOL_F32):
                           ro, rm, rl, tol)
     assert _gpu.row_error(out.cpu().numpy(), ref_out) <= tol
     _gpu.compare_lse(lse.cpu().numpy(), ref_lse, tol)
+    if report:
+        _gpu.report(report, "o_partial", o[:rows].cpu().numpy(), ro)
+        _gpu.report(report, "out", out.cpu().numpy(), ref_out)
 
 
 @pytest.mark.parametrize("split", [0, 2])
@@ -292,28 +295,38 @@ def test_decode_kernel_shapes(bs, ps, qhead, dt):
 TC_SMALL = ["gqa_decode", "chunked_prefill", "chunked_prefill_bf16", "skewed", "long_decode"]
 
 
+TC_PATHS = {"bf16_operands": sa.PATH_TENSOR_CORE, "tf32_scores": sa.PATH_TENSOR_CORE_TF32}
+
+
+@pytest.mark.parametrize("path", list(TC_PATHS), ids=list(TC_PATHS))
 @pytest.mark.parametrize("split", [0, 3, 16])
 @pytest.mark.parametrize("name", TC_SMALL)
-def test_small_workload_tensor_core(name, split):
-    """The tcgen05 kernel on every reduced workload it supports; split 0 puts
-    whole units (more than 128 rows) in one split, so row tiles repeat."""
+def test_small_workload_tensor_core(name, split, path):
+    """The tcgen05 kernel on every reduced workload it supports, with every
+    operand rounded to bf16 (SA_PATH_TENSOR_CORE) and with the scores from
+    Q and K kept f32 (tf32 operands) for f32 K/V (SA_PATH_TENSOR_CORE_TF32);
+    split 0 puts whole units (more than 128 rows) in one split, so row tiles
+    repeat.  The measured errors of both are in the session's report."""
     w = inputs.small(name, seed=2)
-    _check_against_oracle(w, _gpu.device_workload(w), split, sa.PATH_TENSOR_CORE, _gpu.TOL_TC)
+    _check_against_oracle(w, _gpu.device_workload(w), split, TC_PATHS[path], _gpu.TOL_TC,
+                          report=f"small {name} {path} split {split}")
 
 
+@pytest.mark.parametrize("path", list(TC_PATHS), ids=list(TC_PATHS))
 @pytest.mark.parametrize("bs,ps,qhead,dt,causal", [(64, 16, 8, "f32", True),
                                                    (128, 64, 8, "bf16", True),
                                                    (64, 8, 4, "bf16", False),
                                                    (128, 32, 2, "f32", True),
                                                    (64, 64, 1, "f32", False),
-                                                   (128, 16, 16, "bf16", True)])
-def test_tensor_core_shapes(bs, ps, qhead, dt, causal):
+                                                   (128, 16, 16, "bf16", True),
+                                                   (128, 128, 8, "f32", False)])
+def test_tensor_core_shapes(bs, ps, qhead, dt, causal, path):
     w = inputs.chunked_prefill(seed=bs + ps + qhead, batch=3, qo_len=30, kv_len=1500, hkv=2,
                                hq=2 * qhead, head_dim=128, page_size=ps, block_size=bs, topk=5,
                                kv_dtype=dt)
     w.causal = causal
     w.block_tables[1, 2] = -1              # a hole inside a live block
-    _check_against_oracle(w, _gpu.device_workload(w), 7, sa.PATH_TENSOR_CORE, _gpu.TOL_TC)
+    _check_against_oracle(w, _gpu.device_workload(w), 7, TC_PATHS[path], _gpu.TOL_TC)
 
 
 @pytest.mark.parametrize("bs,ps,qhead", [(64, 16, 8), (32, 16, 1), (128, 64, 4), (64, 8, 2),
@@ -338,10 +351,11 @@ def test_tensor_core_bf16_q_copy_matches_f32_gather(name):
     output."""
     w = inputs.small(name, seed=9)
     t = _gpu.device_workload(w)
-    out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=3, path=sa.PATH_TENSOR_CORE)
+    path = sa.PATH_TENSOR_CORE                 # bf16 operands: the path that uses the copy
+    out, lse, idx, (o, m, l) = _gpu.run_attention(w, t, split_edges=3, path=path)
     o2, m2, l2 = sa.sa_forward(t["q"], t["k"], t["v"], idx, t["bt"], t["cu"], t["used"], w.hq,
                                w.hkv, w.head_dim, w.block_size, w.page_size, w.softmax_scale,
-                               w.causal, path=sa.PATH_TENSOR_CORE)
+                               w.causal, path=path)
     assert sa.sa_get_status(idx) == 0
     rows = int(idx.to_host()["edges"].shape[0]) * w.qhead
     assert torch.equal(o[:rows], o2[:rows])
@@ -350,7 +364,7 @@ def test_tensor_core_bf16_q_copy_matches_f32_gather(name):
     out3, lse3, _, _ = sa.sa_attention(q_alias, t["k"], t["v"], t["selected"], w.cu_seqlens_q,
                                        t["cu"], t["used"], t["bt"], w.hq, w.hkv, w.head_dim,
                                        w.block_size, w.page_size, w.softmax_scale, w.causal,
-                                       split_edges=3, out=q_alias, path=sa.PATH_TENSOR_CORE)
+                                       split_edges=3, out=q_alias, path=path)
     torch.cuda.synchronize()
     assert torch.equal(out3, out) and torch.equal(lse3, lse)
 
@@ -397,3 +411,31 @@ def test_attention_graph_replay_unfused(name):
         assert sa.sa_get_status(g.index) == 0
         ref_out, ref_lse, _, _ = _gpu.run_attention(w, t, split_edges=3)
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("topk,split", [(64, 0), (64, 3), (65, 3), (33, 1)])
+def test_decode_index_segment_modes(topk, split):
+    """The index kernel builds segments of at most 64 entries (one query per
+    sequence, topk <= 64: decode batches) one warp each, larger ones through
+    shared-memory histograms; both give the oracle's index bit for bit,
+    with repeated blocks, -1 padding, blocks past the KV length and an empty
+    sequence in the batch."""
+    w = inputs.gqa_decode(seed=topk + split, batch=9, kv_min=4400, kv_max=6000, hq=8, hkv=2,
+                          head_dim=32, topk=topk)
+    rng = np.random.default_rng(topk)
+    sel = w.selected
+    sel[rng.random(sel.shape) < 0.1] = -1
+    sel[2, 0, 5] = sel[2, 0, 7]                      # a block chosen at two ranks
+    sel[4, 1, 3] = w.msb - 1                         # past the sequence's KV length
+    w.qo_lens = w.qo_lens.copy()
+    w.qo_lens[6] = 0                                 # an empty sequence
+    w.selected = np.delete(sel, 6, axis=0)
+    t = {"selected": torch.from_numpy(w.selected).cuda(),
+         "cu": torch.from_numpy(w.cu_seqlens_q).cuda(),
+         "used": torch.from_numpy(w.used_kv_lens).cuda()}
+    idx = sa.sa_build_index(t["selected"], w.cu_seqlens_q, t["cu"], t["used"], w.max_pages,
+                            w.block_size, w.page_size, split_edges=split)
+    assert sa.sa_get_status(idx) == 0
+    ref = oracle.build_index(w.selected, w.cu_seqlens_q, w.used_kv_lens, w.max_pages,
+                             w.block_size, w.page_size, split)
+    _gpu.compare_index(idx.to_host(), ref)
