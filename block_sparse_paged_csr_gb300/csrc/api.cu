@@ -370,6 +370,7 @@ sa_status forward_impl(const float* q, const void* k_pages, const void* v_pages,
         sa::lpt_region(idx->tq, idx->hkv, idx->topk, idx->batch, idx->msb, idx->nbs);
     if (ws_bytes >= lpt.offset + lpt.bytes) {
       a.unit_order = reinterpret_cast<int32_t*>(ws + lpt.offset);
+      a.order_counts = reinterpret_cast<uint32_t*>(ws + lpt.offset + lpt.counts);
       a.max_units = lpt.units;
     }
   }

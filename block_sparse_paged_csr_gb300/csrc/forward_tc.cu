@@ -53,7 +53,6 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;            // rows per MMA tile
-constexpr int kThreads = 640;   // MMA warp, scheduler, 10 loader warps, 2 x 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kTmemCols = 512;  // S[2] at columns 0 / 128, O[2] at 256 / 384
@@ -265,11 +264,25 @@ __device__ __forceinline__ uint2 ld_kv4_bf16(const void* pages, int64_t elem_off
   }
 }
 
-constexpr int kLoaders = 10;         // loader warps 2..11
-constexpr int kLoadThreads = 32 * kLoaders;
-constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;   // 10
-constexpr int kQBatch = kRowsPerLoader;   // Q rows in flight per loader lane
-constexpr int kKvBatch = 13;              // K/V rows in flight per loader warp
+// Warp roles: 0 MMA issue, 1 scheduler, then the loaders, then two softmax /
+// epilogue warpgroups (warp w reads TMEM lanes 32 (w % 4) ..).  Units of
+// 64-key blocks (skewed selections: about one tile each) lean on the
+// loaders' per-unit K/V pass: 14 loaders, 768 threads at 80 registers, S read
+// 32 columns per TMEM load.  Units of 128-key blocks (prefill: many tiles
+// each) lean on the softmax: 10 loaders, 640 threads at 96 registers, S read
+// 64 columns per TMEM load.
+template <int BS> struct TcWarps {
+  static constexpr int kLoaders = BS == 64 ? 14 : 10;
+  static constexpr int kThreads = 32 * (2 + kLoaders + 8);
+  static constexpr int kLoadThreads = 32 * kLoaders;
+  static constexpr int kRowsPerLoader = (kM + kLoaders - 1) / kLoaders;  // Q rows per loader lane
+  static constexpr int kQBatch = kRowsPerLoader;                        // f32 Q rows in flight
+  static constexpr int kKvBatch = (2 * BS + kLoaders - 1) / kLoaders < 13
+                                      ? (2 * BS + kLoaders - 1) / kLoaders : 13;
+  static constexpr int kSoftmaxWarp0 = 2 + kLoaders;
+  static constexpr bool kWideS = BS == 128;
+  static_assert(kSoftmaxWarp0 % 4 == 0, "softmax warpgroups aligned to TMEM lane quarters");
+};
 
 // kTf32: the scores S = Q K^T from Q and K kept in f32 (tcgen05 kind::tf32)
 // instead of rounded to bf16, so their Q and K tiles are twice as large; P
@@ -277,21 +290,15 @@ constexpr int kKvBatch = 13;              // K/V rows in flight per loader warp
 template <int BS, bool kTf32 = false> struct TcCfg {
   static constexpr int E = kTf32 ? 4 : 2;         // bytes per Q / K element
   static constexpr int KVB = kTf32 && BS == 128 ? 1 : 2;     // unit buffers (K, V)
-  static constexpr int NX = kTf32 || BS == 128 ? 1 : 3;     // tile buffers (Q)
+  static constexpr int NX = kTf32 ? 1 : (BS == 128 ? 2 : 3); // tile buffers (Q)
   // epilogue staging tiles per warp: two where shared memory allows (the
   // box store of one drains while the other fills)
-  static constexpr int SB = kTf32 && BS == 128 ? 1 : 2;
+  static constexpr int SB = BS == 64 ? 2 : 1;
 };
 constexpr int kMaxNX = 3;
 constexpr int kRing = 4;                          // unit slots of the scheduler
-// Warp roles: 0 MMA issue, 1 scheduler, 2..11 loaders, 12..19 softmax and
-// epilogue (two warpgroups; warp w reads TMEM lanes 32 (w % 4) ..).  640
-// threads leave 96 registers to each, room for 64 TMEM columns per load.
 constexpr int kSchedWarp = 1;
 constexpr int kLoaderWarp0 = 2;
-constexpr int kSoftmaxWarp0 = kLoaderWarp0 + kLoaders;   // 12
-static_assert(kSoftmaxWarp0 % 4 == 0 && kSoftmaxWarp0 * 32 + 8 * 32 == kThreads,
-              "softmax warpgroups aligned to TMEM lane quarters");
 
 struct UnitInfo {
   int32_t rows;         // edges x qhead of the unit (0: skip)
@@ -359,6 +366,7 @@ struct TcBars {
 };
 
 // OR of `pred` over the loader warps (named barrier 1); also a barrier.
+template <int kLoadThreads>
 __device__ __forceinline__ bool loaders_or(bool pred) {
   uint32_t r;
   asm volatile(
@@ -395,25 +403,6 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
   const int qhead = a.qhead;
   const int ps = a.page_size;
   int64_t* status = a.totals + 3;
-  // The next unit: claimed from the forward's counter (whichever CTA is free
-  // takes the next unit in index order, so heavy units of a skewed selection
-  // do not pile up on a few CTAs), or round-robin without one.  With a
-  // longest-first list the counter walks that list instead.  Each claim is
-  // made one unit ahead, so its round trips overlap the current unit's.
-  auto claim = [&](uint32_t U) -> int64_t {
-    int64_t c = 0;
-    if (lane == 0) {
-      if (a.unit_counter != nullptr) {
-        const uint32_t k = atomicAdd(a.unit_counter, 1u);
-        c = (a.unit_order != nullptr && k < n_units) ? static_cast<int64_t>(a.unit_order[k])
-                                                     : static_cast<int64_t>(k);
-      } else {
-        c = blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
-      }
-    }
-    return c;   // lane 0's value counts
-  };
-  int64_t u_next = claim(0);
   for (uint32_t U = 0;; ++U) {
     const int sl = static_cast<int>(U % kRing);
     unsigned char* slot = smem + P.ring + sl * P.slot_bytes;
@@ -423,7 +412,21 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
       if (lane == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
-    const int64_t u = __shfl_sync(kAll, u_next, 0);
+    // The next unit: claimed from the forward's counter (whichever CTA is
+    // free takes the next unit, so heavy units of a skewed selection do not
+    // pile up on a few CTAs), in the order of the longest-first list when
+    // there is one, else in index order; round-robin without a counter.
+    int64_t u = 0;
+    if (lane == 0) {
+      if (a.unit_counter != nullptr) {
+        const uint32_t k = atomicAdd(a.unit_counter, 1u);
+        u = (a.unit_order != nullptr && k < n_units) ? static_cast<int64_t>(a.unit_order[k])
+                                                     : static_cast<int64_t>(k);
+      } else {
+        u = blockIdx.x + static_cast<int64_t>(U) * gridDim.x;
+      }
+    }
+    u = __shfl_sync(kAll, u, 0);
     if (u >= n_units) {
       // end of work: a unit with rows < 0 tells the other roles to stop
       if (lane == 0) reinterpret_cast<UnitInfo*>(slot)->rows = -1;
@@ -437,7 +440,6 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     else if (lane == 1) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j];
     else if (lane == 2) x = a.sel_offsets[static_cast<int64_t>(h) * (a.nbs + 1) + j + 1];
     else if (lane == 3) x = a.edge_head_base[h];
-    u_next = claim(U + 1);
     const int raw = static_cast<int>(__shfl_sync(kAll, x, 0));
     const int64_t ebase = __shfl_sync(kAll, x, 3);
     const int64_t e0 = ebase + __shfl_sync(kAll, x, 1);
@@ -446,43 +448,31 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     if (bad && lane == 0) report(status, SA_ERR_SHAPE);
     const int b = bad ? 0 : raw / a.msb;
     const int blk = bad ? 0 : raw - b * a.msb;
-    // One round trip for the rest: the sequence's lengths, the block's page
-    // ids and the first tile's query ids are all issued before any is used.
     int64_t y = 0;
     if (lane == 0) y = a.used ? max(a.used[b], 0) : static_cast<int64_t>(a.msb) * BS;
     else if (lane == 1) y = a.cu[b];
     else if (lane == 2) y = a.cu[b + 1];
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
-                        static_cast<int64_t>(blk) * a.pages_per_block;
-    int pid[BS / 32];
-#pragma unroll
-    for (int q = 0; q < BS / 32; ++q) pid[q] = bad ? -1 : bt[(lane + 32 * q) / ps];
-    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
-    int64_t qi[kM / 32];
-#pragma unroll
-    for (int q = 0; q < kM / 32; ++q) {
-      const int r = lane + 32 * q;
-      qi[q] = r < rows ? a.edges[2 * (e0 + r / qhead)] : -1;
-    }
     const int64_t lk = __shfl_sync(kAll, y, 0);
     const int64_t q0 = __shfl_sync(kAll, y, 1);
     const int64_t qo = __shfl_sync(kAll, y, 2) - q0;
+    const int rows = bad ? 0 : static_cast<int>((e1 - e0) * qhead);
     const int64_t bstart = static_cast<int64_t>(blk) * BS;
     const int64_t bend = min(bstart + BS, lk);
     // the keys: position (or -1) and source offset through the block table
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_pages +
+                        static_cast<int64_t>(blk) * a.pages_per_block;
     int64_t* koff = reinterpret_cast<int64_t*>(slot + L::koff);
     int32_t* kpos = reinterpret_cast<int32_t*>(slot + L::kpos);
-#pragma unroll
-    for (int q = 0; q < BS / 32; ++q) {
-      const int jj = lane + 32 * q;
+    for (int jj = lane; jj < BS; jj += 32) {
       const int64_t pos = bstart + jj;
       int32_t live = -1;
       int64_t off = -1;
       if (!bad && pos < bend) {
-        if (pid[q] >= a.num_pages) report(status, SA_ERR_SHAPE);
-        if (pid[q] >= 0 && pid[q] < a.num_pages) {
+        const int pid = bt[jj / ps];
+        if (pid >= a.num_pages) report(status, SA_ERR_SHAPE);
+        if (pid >= 0 && pid < a.num_pages) {
           live = static_cast<int32_t>(pos);
-          off = ((static_cast<int64_t>(pid[q]) * a.hkv + h) * ps + jj % ps) * kD;
+          off = ((static_cast<int64_t>(pid) * a.hkv + h) * ps + jj % ps) * kD;
         }
       }
       kpos[jj] = live;
@@ -490,11 +480,13 @@ __device__ void tc_scheduler(const ForwardArgs& a, unsigned char* smem, const Tc
     }
     // the first tile's Q sources
     int64_t* qsrc = reinterpret_cast<int64_t*>(slot + L::qsrc);
-#pragma unroll
-    for (int q = 0; q < kM / 32; ++q) {
-      const int r = lane + 32 * q;
-      qsrc[r] = qi[q] >= 0 ? (qi[q] * a.hq + static_cast<int64_t>(h) * qhead + r % qhead) * kD
-                           : int64_t{-1};
+    for (int r = lane; r < kM; r += 32) {
+      int64_t src = -1;
+      if (r < rows) {
+        const int64_t qi = a.edges[2 * (e0 + r / qhead)];
+        src = (qi * a.hq + static_cast<int64_t>(h) * qhead + r % qhead) * kD;
+      }
+      qsrc[r] = src;
     }
     if (lane == 0 && a.cta_stats != nullptr && static_cast<int>(blockIdx.x) < a.cta_stats_len) {
       unsigned long long* st = reinterpret_cast<unsigned long long*>(a.cta_stats) + 3 * blockIdx.x;
@@ -524,6 +516,9 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
   constexpr int KVB = TcCfg<BS, kTf32>::KVB;
   constexpr int kNX = TcCfg<BS, kTf32>::NX;
   constexpr int E = TcCfg<BS, kTf32>::E;
+  using W = TcWarps<BS>;
+  constexpr int kLoaders = W::kLoaders, kLoadThreads = W::kLoadThreads;
+  constexpr int kRowsPerLoader = W::kRowsPerLoader, kQBatch = W::kQBatch, kKvBatch = W::kKvBatch;
   using L = SlotLayout<BS>;
   const int lt = lw * 32 + lane;
   const int qhead = a.qhead;
@@ -541,7 +536,7 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
     bool got = mbar_wait_bounded(B.slot_full + sl, (U / kRing) & 1u);
     got = got && (U < static_cast<uint32_t>(KVB) ||
                   mbar_wait_bounded(B.kv_empty + kvb, ((U / KVB) - 1) & 1u));
-    if (loaders_or(!got)) {
+    if (loaders_or<W::kLoadThreads>(!got)) {
       if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
       return;
     }
@@ -646,7 +641,7 @@ __device__ void tc_loader(const ForwardArgs& a, unsigned char* smem, const TcPla
       const int xb = static_cast<int>(T % kNX);
       got = T < static_cast<uint32_t>(kNX) ||
             mbar_wait_bounded(B.x_empty + xb, ((T / kNX) - 1) & 1u);
-      if (loaders_or(!got)) {
+      if (loaders_or<W::kLoadThreads>(!got)) {
         if (lt == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
         return;
       }
@@ -855,7 +850,7 @@ template <int BS, bool kTf32>
 __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsigned char* smem,
                            const TcPlan& P, const TcBars& B, uint32_t tmem, int warp,
                            int lane) {
-  const uint32_t g = static_cast<uint32_t>((warp - kSoftmaxWarp0) >> 2);
+  const uint32_t g = static_cast<uint32_t>((warp - TcWarps<BS>::kSoftmaxWarp0) >> 2);
   constexpr int KVB = TcCfg<BS, kTf32>::KVB;
   int64_t* status = a.totals + 3;
   const int row = (warp & 3) * 32 + lane;               // TMEM lane = tile row
@@ -1029,6 +1024,9 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
       }
       tc_fence_after();
       const uint32_t t_s = tmem + 128 * sb + lane_base;
+      uint64_t l2 = f32x2(0.f, 0.f);          // two partial sums of p
+      float m2;
+      if constexpr (TcWarps<BS>::kWideS) {
       // S in halves of 64 keys, each read with one TMEM load (one round trip):
       // pass 1 takes the row maximum of qscale * s over live keys, as qscale
       // times the largest (qscale >= 0) or smallest raw score (rounding is
@@ -1073,11 +1071,10 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
           }
         }
       }
-      const float m2 = any ? ext * qscale : -INFINITY;
+      m2 = any ? ext * qscale : -INFINITY;
       const float msub = m2 == -INFINITY ? 0.f : m2;
       const uint64_t qs2 = f32x2(qscale, qscale);
       const uint64_t nm2 = f32x2(-msub, -msub);
-      uint64_t l2 = f32x2(0.f, 0.f);          // two partial sums of p
       // P of half hh (v) into pk[32]
       auto p_half = [&](int hh, uint32_t (&pk)[32]) {
 #pragma unroll
@@ -1119,6 +1116,79 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
         p_half(0, pk);
         tmem_st32(t_s, pk);
       }
+      } else {
+      // S 32 keys per TMEM load: pass 1 takes the row maximum of qscale * s
+      // over live keys, as qscale times the largest (qscale >= 0) or
+      // smallest raw score (rounding is monotonic, so the product is the same
+      // maximum; fully live chunks, the common case, without per-key masks,
+      // three scores per instruction); pass 2 reads each chunk again and
+      // writes P as bf16 pairs over the S columns already read (chunk c's 16
+      // columns lie at or before S chunk c).
+      auto live_of = [&](int c) -> uint32_t {      // live keys of 32-key chunk c
+        const int cut = jlim - c * 32;
+        const uint32_t inside = cut >= 31 ? 0xffffffffu : (cut < 0 ? 0u : ((2u << cut) - 1u));
+        return vmask[c] & inside;
+      };
+      const bool up = qscale >= 0.f;
+      float ext = up ? -INFINITY : INFINITY;
+      bool any = false;
+#pragma unroll 1
+      for (int c = 0; c < BS / 32; ++c) {
+        float v[32];
+        tmem_ld32(t_s + c * 32, v);
+        tmem_ld_wait();
+        const uint32_t live = live_of(c);
+        any = any || live != 0u;
+        if (live == 0xffffffffu) {
+          if (up) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) ext = max3(ext, v[i], v[i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) ext = min3(ext, v[i], v[i + 1]);
+          }
+        } else if (live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if ((live >> i) & 1u) ext = up ? fmaxf(ext, v[i]) : fminf(ext, v[i]);
+        }
+      }
+      m2 = any ? ext * qscale : -INFINITY;
+      const float msub = m2 == -INFINITY ? 0.f : m2;
+      const uint64_t qs2 = f32x2(qscale, qscale);
+      const uint64_t nm2 = f32x2(-msub, -msub);
+#pragma unroll 1
+      for (int c = 0; c < BS / 32; ++c) {
+        float v[32];
+        tmem_ld32(t_s + c * 32, v);
+        tmem_ld_wait();
+        const uint32_t live = live_of(c);
+        uint32_t pk[16];
+        if (live == 0xffffffffu) {
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(v[2 * i2], v[2 * i2 + 1]), qs2, nm2), x0, x1);
+            const float p0 = ex2_fast(x0);
+            const float p1 = ex2_fast(x1);
+            l2 = add_f32x2(l2, f32x2(p0, p1));
+            pk[i2] = pack_bf16x2_rn(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int i = 2 * i2;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(v[i], v[i + 1]), qs2, nm2), x0, x1);
+            const float p0 = ((live >> i) & 1u) ? ex2_fast(x0) : 0.f;
+            const float p1 = ((live >> (i + 1)) & 1u) ? ex2_fast(x1) : 0.f;
+            l2 = add_f32x2(l2, f32x2(p0, p1));
+            pk[i2] = pack_bf16x2_rn(p0, p1);
+          }
+        }
+        tmem_st16(t_s + c * 16, pk);
+      }
+      }
       float la, lb;
       f32x2_split(l2, la, lb);
       const float l = la + lb;
@@ -1143,7 +1213,7 @@ __device__ void tc_softmax(const ForwardArgs& a, const CUtensorMap* omap, unsign
 // ------------------------------------------------------------------ kernel
 
 template <int BS, bool kBf16, bool kTf32>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcWarps<BS>::kThreads, 1)
 forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   constexpr int KVB = TcCfg<BS, kTf32>::KVB;
   constexpr int kNX = TcCfg<BS, kTf32>::NX;
@@ -1151,6 +1221,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const TcPlan P = tc_plan<BS, kTf32>();
+  using W = TcWarps<BS>;
+  constexpr int kLoadThreads = W::kLoadThreads;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   TcBars B;
   B.kv_full = bars;
@@ -1216,7 +1288,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int64_t n_units = unit_base[a.hkv];
-  if (warp >= kSoftmaxWarp0) {
+  if (warp >= W::kSoftmaxWarp0) {
     tc_softmax<BS, kTf32>(a, &omap, smem, P, B, tmem, warp, lane);
     // box stores issued by this thread have landed before the CTA leaves
     bulk_wait_all();
@@ -1244,24 +1316,43 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
 }
 
 // The longest-first work list: every unit (kv head, compact slot) of the
-// index, numbered across heads as the scheduler numbers them, in classes of
-// descending size (class c: 2^c <= edges < 2^(c+1), the last class open),
-// largest class first.  Inside a class each warp places its 32 consecutive
-// units together, in index order, with one atomic per warp and class, so
-// runs of neighbouring blocks (which share their queries' Q rows in L2) stay
-// together; which run comes first is not fixed, which changes which CTA runs
-// a unit but no result.  One CTA: the list is a few tens of thousands of
-// entries at most.
+// index, numbered across heads as the scheduler numbers them.  Cost model:
+// a unit costs about its edges (each edge is qhead rows of the tile loop);
+// a unit whose cost reaches an eighth of a CTA's mean share (E / ctas / 8
+// edges) is heavy and could leave the SMs idle behind it if claimed late,
+// so heavy units come first, in classes of descending size (2^c <= edges <
+// 2^(c+1)); the light rest keep index order, where neighbouring blocks,
+// claimed at the same time by different CTAs, share their queries' Q rows
+// in L2 (an order by size alone scattered them and cost more than it
+// balanced).  Inside a class, index order.  Two kernels over the same grid
+// of 1024-unit chunks: the first counts each chunk's units per class, the
+// second places each chunk's units after the larger classes and after the
+// earlier chunks' units of its class, warp by warp, lane by lane.
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderClasses = 16;
-constexpr int kOrderBatch = 8;     // units whose counts are in flight per thread
 
-__global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a) {
-  __shared__ int32_t ubase[201];
-  __shared__ uint32_t cursor[kOrderClasses];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  if (tid == 0) {
+// Unit u's class (-1 past the end) from the per-head unit bases: 0 for a
+// light unit, 1 + floor(log2(edges)) (at most the last class) for a heavy one.
+__device__ __forceinline__ int unit_class(const ForwardArgs& a, const int32_t* ubase, int64_t n,
+                                          int64_t u, int64_t heavy) {
+  if (u >= n) return -1;
+  int h = 0;
+  while (h + 1 < a.hkv && ubase[h + 1] <= u) ++h;
+  const int32_t* off = a.sel_offsets + static_cast<int64_t>(h) * (a.nbs + 1) + (u - ubase[h]);
+  const int c = max(off[1] - off[0], 1);
+  if (c < heavy) return 0;
+  return min(1 + 31 - __clz(c), kOrderClasses - 1);
+}
+
+// Edges from which a unit is heavy: an eighth of a CTA's mean share.
+__device__ __forceinline__ int64_t heavy_edges(const ForwardArgs& a) {
+  const int64_t e = a.totals[0] > 0 ? a.totals[0] : 0;
+  const int64_t share = e / (8 * static_cast<int64_t>(a.order_ctas > 0 ? a.order_ctas : 1));
+  return share > 1 ? share : 1;
+}
+
+__device__ __forceinline__ int64_t order_unit_bases(const ForwardArgs& a, int32_t* ubase) {
+  if (threadIdx.x == 0) {
     int32_t acc = 0;
     for (int hh = 0; hh < a.hkv; ++hh) {
       ubase[hh] = acc;
@@ -1269,71 +1360,66 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a
     }
     ubase[a.hkv] = acc > a.max_units ? static_cast<int32_t>(a.max_units) : acc;
   }
-  if (tid < kOrderClasses) cursor[tid] = 0;
   __syncthreads();
-  const int64_t n = ubase[a.hkv];
-  // class of unit u, -1 past the end: floor(log2(edges)), at most the last
-  auto classes_of = [&](int64_t u0, int (&cls)[kOrderBatch]) {
-    int32_t lo[kOrderBatch], hi[kOrderBatch];
-#pragma unroll
-    for (int q = 0; q < kOrderBatch; ++q) {
-      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
-      lo[q] = hi[q] = 0;
-      if (u < n) {
-        int h = 0;
-        while (h + 1 < a.hkv && ubase[h + 1] <= u) ++h;
-        const int32_t* off = a.sel_offsets + static_cast<int64_t>(h) * (a.nbs + 1) + (u - ubase[h]);
-        lo[q] = off[0];
-        hi[q] = off[1];
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kOrderBatch; ++q) {
-      const int64_t u = u0 + static_cast<int64_t>(q) * kOrderThreads;
-      const int c = max(hi[q] - lo[q], 1);
-      cls[q] = u < n ? min(31 - __clz(c), kOrderClasses - 1) : -1;
-    }
-  };
-  const int64_t step = static_cast<int64_t>(kOrderThreads) * kOrderBatch;
-  // pass 1: class sizes (one shared-memory atomic per warp and class
-  // present); their exclusive prefix, largest class first
-  for (int64_t u0 = tid - lane; u0 < n; u0 += step) {
-    int cls[kOrderBatch];
-    classes_of(u0 + lane, cls);
-#pragma unroll
-    for (int q = 0; q < kOrderBatch; ++q) {
-      const unsigned peers = __match_any_sync(0xffffffffu, cls[q]);
-      if (cls[q] >= 0 && lane == __ffs(peers) - 1)
-        atomicAdd(&cursor[cls[q]], static_cast<uint32_t>(__popc(peers)));
+  return ubase[a.hkv];
+}
+
+// counts[chunk][class] of the chunk's units
+__global__ void __launch_bounds__(kOrderThreads) unit_class_count_kernel(ForwardArgs a) {
+  __shared__ int32_t ubase[201];
+  __shared__ uint32_t cnt[kOrderClasses];
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < kOrderClasses) cnt[tid] = 0;
+  const int64_t n = order_unit_bases(a, ubase);
+  const int c = unit_class(a, ubase, n, static_cast<int64_t>(blockIdx.x) * kOrderThreads + tid,
+                          heavy_edges(a));
+  const unsigned peers = __match_any_sync(0xffffffffu, c);
+  if (c >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[c], static_cast<uint32_t>(__popc(peers)));
+  __syncthreads();
+  if (tid < kOrderClasses) a.order_counts[blockIdx.x * kOrderClasses + tid] = cnt[tid];
+}
+
+__global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(ForwardArgs a) {
+  __shared__ int32_t ubase[201];
+  __shared__ uint32_t base[kOrderClasses], total[kOrderClasses], before[kOrderClasses];
+  __shared__ uint32_t wcnt[kOrderThreads / 32][kOrderClasses];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < kOrderClasses) total[tid] = before[tid] = 0;
+  const int64_t n = order_unit_bases(a, ubase);
+  // every chunk's class counts: per class the total, and the earlier chunks'
+  for (int64_t e = tid; e < static_cast<int64_t>(gridDim.x) * kOrderClasses; e += kOrderThreads) {
+    const uint32_t x = a.order_counts[e];
+    const int cc = static_cast<int>(e % kOrderClasses);
+    if (x) {
+      atomicAdd(&total[cc], x);
+      if (e / kOrderClasses < blockIdx.x) atomicAdd(&before[cc], x);
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    uint32_t run = 0;
-    for (int c = kOrderClasses - 1; c >= 0; --c) {
-      const uint32_t x = cursor[c];
-      cursor[c] = run;
+  if (tid < kOrderClasses) {
+    uint32_t larger = 0;
+    for (int cc = tid + 1; cc < kOrderClasses; ++cc) larger += total[cc];
+    base[tid] = larger + before[tid];
+  }
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kOrderThreads + tid;
+  const int c = unit_class(a, ubase, n, u, heavy_edges(a));
+  // rank among the warp's units of the same class, and the warp's counts
+  const unsigned peers = __match_any_sync(0xffffffffu, c);
+  const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
+  if (lane < kOrderClasses) wcnt[warp][lane] = 0;
+  __syncwarp();
+  if (c >= 0 && lane == __ffs(peers) - 1) wcnt[warp][c] = __popc(peers);
+  __syncthreads();
+  if (tid < kOrderClasses) {
+    uint32_t run = base[tid];
+    for (int w = 0; w < kOrderThreads / 32; ++w) {
+      const uint32_t x = wcnt[w][tid];
+      wcnt[w][tid] = run;
       run += x;
     }
   }
   __syncthreads();
-  // pass 2: each warp's runs of 32 consecutive units, class by class
-  for (int64_t u0 = tid - lane; u0 < n; u0 += step) {
-    int cls[kOrderBatch];
-    classes_of(u0 + lane, cls);
-#pragma unroll
-    for (int q = 0; q < kOrderBatch; ++q) {
-      const int64_t u = u0 + lane + static_cast<int64_t>(q) * kOrderThreads;
-      const unsigned peers = __match_any_sync(0xffffffffu, cls[q]);
-      const int leader = __ffs(peers) - 1;
-      uint32_t base = 0;
-      if (cls[q] >= 0 && lane == leader)
-        base = atomicAdd(&cursor[cls[q]], static_cast<uint32_t>(__popc(peers)));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      if (cls[q] >= 0)
-        a.unit_order[base + __popc(peers & ((1u << lane) - 1u))] = static_cast<int32_t>(u);
-    }
-  }
+  if (c >= 0) a.unit_order[wcnt[warp][c] + rank] = static_cast<int32_t>(u);
 }
 
 template <int BS, bool kBf16, bool kTf32>
@@ -1375,17 +1461,20 @@ cudaError_t launch_tc(const ForwardArgs& a, cudaStream_t stream) {
   } else {
     args.unit_order = nullptr;
   }
-  if (args.unit_order != nullptr) {
-    unit_order_kernel<<<1, kOrderThreads, 0, stream>>>(args);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   // One CTA per SM: it holds all 512 TMEM columns.
   int64_t grid = device_sm_count();
   if (grid > a.max_splits) grid = a.max_splits;
   if (grid < 1) grid = 1;
+  args.order_ctas = static_cast<int32_t>(grid);
+  if (args.unit_order != nullptr) {
+    const unsigned chunks = static_cast<unsigned>((args.max_units + kOrderThreads - 1) / kOrderThreads);
+    unit_class_count_kernel<<<chunks, kOrderThreads, 0, stream>>>(args);
+    unit_order_kernel<<<chunks, kOrderThreads, 0, stream>>>(args);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   forward_tc_kernel<BS, kBf16, kTf32>
-      <<<static_cast<unsigned>(grid), kThreads, p.total, stream>>>(omap, args);
+      <<<static_cast<unsigned>(grid), TcWarps<BS>::kThreads, p.total, stream>>>(omap, args);
   return cudaGetLastError();
 }
 

@@ -738,7 +738,9 @@ LptRegion lpt_region(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32
   LptRegion r;
   r.units = units > 0 ? units : 1;
   r.offset = (build + 255) & ~static_cast<size_t>(255);
-  r.bytes = (4 * static_cast<size_t>(units > 0 ? units : 1) + 255) & ~static_cast<size_t>(255);
+  r.counts = (4 * static_cast<size_t>(r.units) + 255) & ~static_cast<size_t>(255);
+  const size_t chunks = (static_cast<size_t>(r.units) + 1023) / 1024;
+  r.bytes = r.counts + ((64 * chunks + 255) & ~static_cast<size_t>(255));
   return r;
 }
 
@@ -765,7 +767,10 @@ cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
   // work items: chunks, or in warp-per-segment mode warps' worth of segments
   const int64_t items =
       a.small ? (static_cast<int64_t>(a.hkv) * a.batch + kWarps - 1) / kWarps : n_chunks;
-  const int64_t want = std::max<int64_t>(std::max<int64_t>(items, plateau_ctas), 1);
+  int64_t want = std::max<int64_t>(std::max<int64_t>(items, plateau_ctas), 1);
+  // warp-per-segment mode: one CTA per SM at most (a smaller barrier; the
+  // plateau is then a few dozen coalesced stores per thread)
+  if (a.small) want = std::max<int64_t>(items, std::min<int64_t>(want, device_sm_count()));
   if (grid > want) grid = want;
   IndexArgs args = a;
   int site = kStallNone;

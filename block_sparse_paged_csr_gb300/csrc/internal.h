@@ -35,7 +35,8 @@ WorkspaceLayout workspace_layout(int32_t hkv, int32_t batch, int64_t tq,
 // after everything an index build of these sizes may use: `offset` bytes
 // from the workspace start, `bytes` long (int32 per possible work unit).
 struct LptRegion {
-  size_t offset, bytes;
+  size_t offset, bytes;     // the list (int32 per unit), then the sort's counts
+  size_t counts;            // offset of the counts from `offset`
   int64_t units;
 };
 LptRegion lpt_region(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32_t msb,
@@ -109,6 +110,8 @@ struct ForwardArgs {
                             // index workspace): the launcher writes the units there in
                             // longest-first order and the counter walks that list
   int64_t max_units;        // entries unit_order has room for
+  uint32_t* order_counts;   // [ceil(max_units / 1024)][16] scratch of the list's sort
+  int32_t order_ctas;       // CTAs of the forward (the list's cost model)
   int64_t* cta_stats;       // nullable (test hook): per CTA rows, units, busy cycles
   int32_t cta_stats_len;    // CTAs cta_stats has room for
   float* m_partial;

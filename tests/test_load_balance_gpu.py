@@ -3,7 +3,9 @@ longest-first claiming).
 
 The forward.rs page walks its WorkSplit list with a thread pool; here the
 units (kv head, block) are claimed by persistent CTAs from a counter that
-walks the units sorted by descending edge count.  On a skewed selection
+walks a list with the heavy units (an eighth of a CTA's mean share of edges
+or more) first, by descending size class, and the light rest in index
+order.  On a skewed selection
 (Zipf block popularity: a few units with hundreds of edges, many with a few)
 the test reads back each CTA's claimed rows and busy cycles
 (sa_debug_cta_stats) with the longest-first list and with plain index order,
