@@ -500,15 +500,20 @@ sa_status sa_combine(const sa_index* idx, const float* o_partial, const float* m
                        stream);
 }
 
-sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void* v_pages,
-                                int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
-                                const int32_t* selected, const int64_t* cu_seqlens_q_host,
-                                const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
-                                const int32_t* block_tables, int32_t hq, int32_t head_dim,
-                                int32_t block_size, int32_t page_size, float softmax_scale,
-                                int32_t causal, int32_t split_edges, sa_dtype partial_dtype,
-                                void* o_partial, float* m_partial, float* l_partial, float* out,
-                                float* lse, sa_path path, void* stream) {
+namespace {
+
+// Steps 2 and 3.  `behind_build`: the index build that made `idx` was the
+// last launch on `stream` (sa_attention), so the fused decode kernel may be
+// launched as its programmatic dependent.
+sa_status forward_combine_impl(const float* q, const void* k_pages, const void* v_pages,
+                               int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                               const int32_t* selected, const int64_t* cu_seqlens_q_host,
+                               const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                               const int32_t* block_tables, int32_t hq, int32_t head_dim,
+                               int32_t block_size, int32_t page_size, float softmax_scale,
+                               int32_t causal, int32_t split_edges, sa_dtype partial_dtype,
+                               void* o_partial, float* m_partial, float* l_partial, float* out,
+                               float* lse, sa_path path, void* stream, bool behind_build) {
   if (idx == nullptr) return SA_ERR_INVALID_ARGUMENT;
   if (partial_dtype != SA_DTYPE_F32 && partial_dtype != SA_DTYPE_BF16)
     return SA_ERR_INVALID_ARGUMENT;
@@ -618,10 +623,29 @@ sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void*
   a.part_l = l_partial;
   a.out = out;
   a.lse = lse;
+  a.pdl = behind_build ? 1 : 0;
   (void)causal;   // a no-op for one query per sequence (its position is lk - 1)
   const cudaError_t err = sa::launch_fused_dec(a, static_cast<cudaStream_t>(stream));
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // namespace
+
+sa_status sa_forward_combine_ex(const float* q, const void* k_pages, const void* v_pages,
+                                int64_t num_pages, sa_dtype kv_dtype, const sa_index* idx,
+                                const int32_t* selected, const int64_t* cu_seqlens_q_host,
+                                const int64_t* cu_seqlens_q, const int32_t* used_kv_lens,
+                                const int32_t* block_tables, int32_t hq, int32_t head_dim,
+                                int32_t block_size, int32_t page_size, float softmax_scale,
+                                int32_t causal, int32_t split_edges, sa_dtype partial_dtype,
+                                void* o_partial, float* m_partial, float* l_partial, float* out,
+                                float* lse, sa_path path, void* stream) {
+  return forward_combine_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                              cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                              head_dim, block_size, page_size, softmax_scale, causal, split_edges,
+                              partial_dtype, o_partial, m_partial, l_partial, out, lse, path,
+                              stream, false);
 }
 
 sa_status sa_forward_combine(const float* q, const void* k_pages, const void* v_pages,
@@ -673,11 +697,11 @@ sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pag
                                       batch, used_kv_lens, max_pages, block_size, page_size,
                                       split_edges, idx, stream);
   if (st != SA_OK) return st;
-  return sa_forward_combine_ex(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
-                               cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
-                               head_dim, block_size, page_size, softmax_scale, causal,
-                               split_edges, partial_dtype, o_partial, m_partial, l_partial, out,
-                               lse, path, stream);
+  return forward_combine_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                              cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                              head_dim, block_size, page_size, softmax_scale, causal, split_edges,
+                              partial_dtype, o_partial, m_partial, l_partial, out, lse, path,
+                              stream, true);
 }
 
 sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,

@@ -1347,7 +1347,7 @@ __device__ __forceinline__ int unit_class(const ForwardArgs& a, const int32_t* u
 // Edges from which a unit is heavy: an eighth of a CTA's mean share.
 __device__ __forceinline__ int64_t heavy_edges(const ForwardArgs& a) {
   const int64_t e = a.totals[0] > 0 ? a.totals[0] : 0;
-  const int64_t share = e / (8 * static_cast<int64_t>(a.order_ctas > 0 ? a.order_ctas : 1));
+  const int64_t share = e / (32 * static_cast<int64_t>(a.order_ctas > 0 ? a.order_ctas : 1));
   return share > 1 ? share : 1;
 }
 

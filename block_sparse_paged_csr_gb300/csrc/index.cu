@@ -57,17 +57,28 @@ __device__ __forceinline__ int64_t splits_of(int64_t count, int split_edges) {
 // Grid-wide barrier for a cooperative launch.  The last CTA to arrive first
 // runs `last` (with all of its threads), then resets the counter and bumps the
 // generation; the others spin (bounded) on the generation.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Grid-wide barrier for a cooperative launch.  `gen0` is the generation read
+// (by thread 0) at the start of the kernel: no CTA can pass this barrier
+// before every CTA has arrived, so it cannot have moved since.  Arrival is an
+// acquire-release add (the CTA's earlier writes, fenced by each thread, go
+// first; the last arrival sees everyone's);
+// the last CTA to arrive first runs `last` (with all of its threads), then
+// resets the counter and publishes the next generation with a release store;
+// the others poll the generation (acquire, bounded).
 template <typename F>
-__device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, uint32_t limit,
-                             bool stall, F last) {
+__device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t gen0, uint32_t nblocks,
+                             uint32_t limit, bool stall, F last) {
   __shared__ int s_ok, s_last;
-  __shared__ uint32_t s_gen;
   __syncthreads();
   if (threadIdx.x == 0) {
     s_ok = 1;
-    s_gen = ld_acquire_u32(gen);
-    __threadfence();
-    s_last = atomicAdd(count, 1u) == nblocks - 1;
+    s_last = atom_add_acq_rel_u32(count, 1u) == nblocks - 1;
     if (stall) s_last = 0;   // test hook: nobody releases the barrier
   }
   __syncthreads();
@@ -76,18 +87,17 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t nblocks, u
     last();
     __syncthreads();
     if (threadIdx.x == 0) {
-      atomicExch(count, 0u);
-      __threadfence();
-      st_release_u32(gen, s_gen + 1);
+      *reinterpret_cast<volatile uint32_t*>(count) = 0u;
+      st_release_u32(gen, gen0 + 1);
     }
   } else if (threadIdx.x == 0) {
     uint32_t it = 0;
-    while (ld_acquire_u32(gen) == s_gen) {
+    while (ld_acquire_u32(gen) == gen0) {
       if (++it > limit) {
         s_ok = 0;
         break;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
   }
   __syncthreads();
@@ -155,6 +165,7 @@ struct Shared {
   int32_t nch_head;      // chunks per head
   int32_t nmulti_head;   // histogram slots per head
   int last;
+  uint32_t gen0;         // barrier generation at the start
 };
 
 // Which (head, sequence, chunk) a chunk id names.
@@ -174,55 +185,115 @@ __device__ __forceinline__ void locate(int64_t c, const int32_t* chunk_base, int
 // ---- warp-per-segment mode (every segment holds at most 64 entries) --------
 // Entry t of segment (h, b) (query cu[b] + t / topk, rank t % topk) sits in
 // lane t & 31 of round t >> 5.  With 64 entries at most, every statistic of
-// the counting sort comes from one pass of warp shuffles over the entries:
-// for entry t with block x (kept entries only),
+// the counting sort comes from warp shuffles over the entries: for entry t
+// with block x (kept entries only),
 //   same   kept entries with block x,
 //   before kept entries with block x and a smaller t (0: t opens its bucket),
-//   less   kept entries with a smaller block.
+//   less   kept entries with a smaller block,
+//   ul     buckets (distinct blocks) below x, sl their work splits.
+// All of it is local to the segment, so a warp computes it before the grid
+// barrier and keeps it in registers for the scatter after it.
 struct SmallSeg {
+  int64_t q0;        // first query of the sequence
+  int n;             // entries of the segment
+  bool bad;          // an out-of-range block id was seen
   int blk[2];        // block of the entry, -1 when dropped
-  int same[2], before[2], less[2];
+  int same[2], before[2], less[2], ul[2], sl[2];
 };
 
 __device__ __forceinline__ void small_segment(const IndexArgs& a, int h, int b, int lane,
-                                              bool check, int64_t* status, SmallSeg& g,
-                                              int& n_out) {
-  const int64_t q0 = a.cu[b];
-  const int n = static_cast<int>((a.cu[b + 1] - q0) * a.topk);
+                                              SmallSeg& g) {
+  g.q0 = a.cu[b];
+  g.n = static_cast<int>((a.cu[b + 1] - g.q0) * a.topk);
+  const int n = g.n;
   const int64_t lk = a.used ? (a.used[b] > 0 ? a.used[b] : 0)
                             : static_cast<int64_t>(a.msb) * a.block_size;
+  g.bad = false;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int t = 32 * k + lane;
     g.blk[k] = -1;
     if (t < n) {
-      const int64_t i = q0 + t / a.topk;
+      const int64_t i = g.q0 + t / a.topk;
       const int r = t % a.topk;
       const int x = a.selected[(i * a.hkv + h) * a.topk + r];
-      if (check && (x < -1 || x >= a.msb)) report(status, SA_ERR_SELECTED_RANGE);
+      if (x < -1 || x >= a.msb) g.bad = true;
       if (x >= 0 && x < a.msb && static_cast<int64_t>(x) * a.block_size < lk) g.blk[k] = x;
     }
-    g.same[k] = g.before[k] = g.less[k] = 0;
+    g.same[k] = g.before[k] = g.less[k] = g.ul[k] = 0;
+    g.sl[k] = 0;
   }
-  for (int j = 0; j < n; ++j) {
-    const int xj = __shfl_sync(0xffffffffu, j < 32 ? g.blk[0] : g.blk[1], j & 31);
-    if (xj < 0) continue;
+  // Both rounds' entry j at once (j < 32): independent shuffles, unrolled so
+  // that their latencies overlap.
+  const int nj = n < 32 ? n : 32;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j >= nj) break;
+    const int x0 = __shfl_sync(0xffffffffu, g.blk[0], j);
+    const int x1 = __shfl_sync(0xffffffffu, g.blk[1], j);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int t = 32 * k + lane;
-      if (g.blk[k] < 0) continue;
-      if (xj == g.blk[k]) {
-        ++g.same[k];
-        if (j < t) ++g.before[k];
-      } else if (xj < g.blk[k]) {
-        ++g.less[k];
-      }
+      const int x = g.blk[k];
+      // entry j (round 0) and entry 32 + j (round 1)
+      const int e0 = (x0 >= 0 && x >= 0) ? (x0 == x ? 1 : 0) : 0;
+      const int e1 = (x1 >= 0 && x >= 0) ? (x1 == x ? 1 : 0) : 0;
+      g.same[k] += e0 + e1;
+      g.before[k] += (j < t ? e0 : 0) + (32 + j < t ? e1 : 0);
+      g.less[k] += (x0 >= 0 && x >= 0 && x0 < x ? 1 : 0) +
+                   (x1 >= 0 && x >= 0 && x1 < x ? 1 : 0);
     }
   }
-  n_out = n;
+  // Buckets below each entry's block: the opening entries (before == 0) of
+  // smaller blocks, and their splits.  When no block repeats (one query per
+  // sequence, as in decode), every kept entry opens its bucket of one edge:
+  // both are `less`.
+  const bool repeats = (g.blk[0] >= 0 && g.same[0] > 1) || (g.blk[1] >= 0 && g.same[1] > 1);
+  if (!__any_sync(0xffffffffu, repeats)) {
+    const int one = static_cast<int>(splits_of(1, a.split_edges));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      g.ul[k] = g.less[k];
+      g.sl[k] = g.less[k] * one;
+    }
+    return;
+  }
+#pragma unroll 4
+  for (int j = 0; j < nj; ++j) {
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int xj = __shfl_sync(0xffffffffu, g.blk[kk], j);
+      const int bj = __shfl_sync(0xffffffffu, g.before[kk], j);
+      const int sj = __shfl_sync(0xffffffffu, g.same[kk], j);
+      const bool open = xj >= 0 && bj == 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (open && g.blk[k] >= 0 && xj < g.blk[k]) {
+          ++g.ul[k];
+          g.sl[k] += static_cast<int>(splits_of(sj, a.split_edges));
+        }
+    }
+  }
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+// Fill p[0, n) with v over all threads of the grid (16-byte stores on the
+// aligned middle).
+__device__ __forceinline__ void fill_i32(int32_t* p, int64_t n, int32_t v, int64_t tid,
+                                         int64_t nthreads) {
+  if (n <= 0) return;
+  const int64_t mis = static_cast<int64_t>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+  const int64_t head = mis ? (4 - mis < n ? 4 - mis : n) : 0;
+  if (tid < head) p[tid] = v;
+  int4* q = reinterpret_cast<int4*>(p + head);
+  const int64_t nv = (n - head) >> 2;
+  const int4 w = make_int4(v, v, v, v);
+  for (int64_t i = tid; i < nv; i += nthreads) q[i] = w;
+  const int64_t tail = head + 4 * nv;
+  if (tid < n - tail) p[tail + tid] = v;
+}
+
+template <bool kSmall>
+__global__ void __launch_bounds__(kThreads, kSmall ? 2 : 4)
 index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   extern __shared__ int64_t dyn64[];
   const int msb = a.msb;
@@ -255,7 +326,7 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   // chunk_base[b]: chunks of the sequences before b; multi_base[b]: the same
   // over sequences of several chunks.  One block scan per kThreads sequences
   // (the cu reads of a tile are issued together, not one after another).
-  if (!a.small) {
+  if (!kSmall) {
     int64_t carry_c = 0, carry_m = 0;
     for (int base = 0; base < batch; base += kThreads) {
       const int b = base + tid;
@@ -282,6 +353,7 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
       s.nmulti_head = static_cast<int32_t>(carry_m);
     }
   }
+  if (tid == 0) s.gen0 = ld_acquire_u32(bar_gen);
   if (blockIdx.x == 0 && tid == 0) {
     *status = 0;
     __threadfence();
@@ -295,36 +367,36 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   const int nmulti = s.nmulti_head;
 
   // ---- phase 1: per-chunk histograms and segment totals ---------------------
-  if (a.small) {
-    // one warp per segment (segments spread over the CTAs first, then over
-    // their warps): kept entries, distinct blocks, work splits
-    for (int seg = warp * gridDim.x + blockIdx.x; seg < nseg; seg += gridDim.x * kWarps) {
-      const int h = seg / batch, b = seg - (seg / batch) * batch;
-      SmallSeg g;
-      int n = 0;
-      small_segment(a, h, b, lane, false, status, g, n);
-      int64_t v[3] = {0, 0, 0};
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
+  const int64_t gthreads = static_cast<int64_t>(gridDim.x) * kThreads;
+  // Warp-per-segment mode: one segment per warp at most (the launch has
+  // enough warps), spread over the CTAs first, then over their warps.
+  const int my_seg = warp * gridDim.x + blockIdx.x;
+  SmallSeg g;
+  if (kSmall && my_seg < nseg) {
+    const int h = my_seg / batch, b = my_seg - (my_seg / batch) * batch;
+    small_segment(a, h, b, lane, g);
+    int64_t v[3] = {0, 0, 0};
 #pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (g.blk[k] >= 0) {
-          v[0] += 1;
-          if (g.before[k] == 0) {
-            v[1] += 1;
-            v[2] += splits_of(g.same[k], a.split_edges);
-          }
+    for (int k = 0; k < 2; ++k)
+      if (g.blk[k] >= 0) {
+        v[0] += 1;
+        if (g.before[k] == 0) {
+          v[1] += 1;
+          v[2] += splits_of(g.same[k], a.split_edges);
         }
-#pragma unroll
-      for (int q = 0; q < 3; ++q)
-#pragma unroll
-        for (int off = 16; off; off >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
-      if (lane == 0) {
-        seg_tot[3 * seg + 0] = static_cast<int32_t>(v[0]);
-        seg_tot[3 * seg + 1] = static_cast<int32_t>(v[1]);
-        seg_tot[3 * seg + 2] = static_cast<int32_t>(v[2]);
       }
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+    if (lane == 0) {
+      seg_tot[3 * my_seg + 0] = static_cast<int32_t>(v[0]);
+      seg_tot[3 * my_seg + 1] = static_cast<int32_t>(v[1]);
+      seg_tot[3 * my_seg + 2] = static_cast<int32_t>(v[2]);
     }
   }
-  for (int64_t c = a.small ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
+  for (int64_t c = kSmall ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
     int h, b, k;
     locate(c, chunk_base, batch, nch_head, h, b, k);
     const int nc = chunk_base[b + 1] - chunk_base[b];
@@ -384,41 +456,68 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
     __syncthreads();
   }
   // Segments without entries have no chunk: their totals are zero.
-  for (int64_t g = a.small ? nseg : static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < nseg;
-       g += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int b = static_cast<int>(g % batch);
+  for (int64_t sg = kSmall ? nseg : gtid; sg < nseg; sg += gthreads) {
+    const int b = static_cast<int>(sg % batch);
     if (chunk_base[b + 1] == chunk_base[b]) {
-      seg_tot[3 * g + 0] = 0;
-      seg_tot[3 * g + 1] = 0;
-      seg_tot[3 * g + 2] = 0;
+      seg_tot[3 * sg + 0] = 0;
+      seg_tot[3 * sg + 1] = 0;
+      seg_tot[3 * sg + 2] = 0;
     }
   }
 
   __threadfence();
   // The last CTA to finish phase 1 turns the segment totals into exclusive
   // prefixes (edges, non-empty bins, splits) for everyone.
+  // Each thread takes a run of consecutive segments: all their totals are
+  // loaded at once (held in registers for up to kKeep segments a thread), one
+  // block scan, then the run's prefixes.
   auto scan_segments = [&]() {
-    int64_t carry[3] = {0, 0, 0};
-    for (int base = 0; base < nseg; base += kThreads) {
-      const int q = base + tid;
-      int64_t v[3] = {0, 0, 0};
-      if (q < nseg)
+    constexpr int kKeep = 4;
+    const int per = (nseg + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, nseg);
+    const int hi = min(lo + per, nseg);
+    const volatile int32_t* tot_v = seg_tot;
+    int32_t keep[kKeep][3];
+    int64_t v[3] = {0, 0, 0};
+    if (per <= kKeep) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j) v[j] = *reinterpret_cast<volatile int32_t*>(seg_tot + 3 * q + j);
-      int64_t excl[3], tot[3];
-      block_scan3(v, excl, tot, s.scratch);
-      if (q < nseg)
+      for (int u = 0; u < kKeep; ++u)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) seg_pre[3 * q + j] = carry[j] + excl[j];
+        for (int j = 0; j < 3; ++j) keep[u][j] = lo + u < hi ? tot_v[3 * (lo + u) + j] : 0;
 #pragma unroll
-      for (int j = 0; j < 3; ++j) carry[j] += tot[j];
+      for (int u = 0; u < kKeep; ++u)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) v[j] += keep[u][j];
+    } else {
+      for (int q = lo; q < hi; ++q)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) v[j] += tot_v[3 * q + j];
+    }
+    int64_t excl[3], tot[3];
+    block_scan3(v, excl, tot, s.scratch);
+    if (per <= kKeep) {
+#pragma unroll
+      for (int u = 0; u < kKeep; ++u)
+        if (lo + u < hi)
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            seg_pre[3 * (lo + u) + j] = excl[j];
+            excl[j] += keep[u][j];
+          }
+    } else {
+      for (int q = lo; q < hi; ++q)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          seg_pre[3 * q + j] = excl[j];
+          excl[j] += tot_v[3 * q + j];
+        }
     }
     if (tid == 0)
 #pragma unroll
-      for (int j = 0; j < 3; ++j) seg_pre[3 * nseg + j] = carry[j];
+      for (int j = 0; j < 3; ++j) seg_pre[3 * nseg + j] = tot[j];
     __threadfence();
   };
-  if (!grid_barrier(bar_count, bar_gen, gridDim.x, a.spin_limit ? a.spin_limit : kSpinLimit,
+  if (!grid_barrier(bar_count, bar_gen, s.gen0, gridDim.x, a.spin_limit ? a.spin_limit : kSpinLimit,
                     a.stall != 0, scan_segments)) {
     if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
     return;
@@ -433,84 +532,61 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   __syncthreads();
 
   // ---- phase 2: prefixes, slot writes, stable scatter ----------------------
-  if (a.small) {
-    // one warp per segment: entry t goes to edge pre + less + before (blocks
-    // ascending, (query, rank) ascending inside a block); the entry that
-    // opens a bucket writes its compact slot and its work splits, placed by
-    // the buckets of smaller blocks (ranks among the opening entries)
-    for (int seg = warp * gridDim.x + blockIdx.x; seg < nseg; seg += gridDim.x * kWarps) {
-      const int h = seg / batch, b = seg - (seg / batch) * batch;
-      SmallSeg g;
-      int n = 0;
-      small_segment(a, h, b, lane, true, status, g, n);
-      int64_t pre[3];
+  if (kSmall && my_seg < nseg) {
+    // one warp per segment, from the registers of phase 1: entry t goes to
+    // edge pre + less + before (blocks ascending, (query, rank) ascending
+    // inside a block); the entry that opens a bucket writes its compact slot
+    // and its work splits, placed by the buckets of smaller blocks
+    const int h = my_seg / batch, b = my_seg - (my_seg / batch) * batch;
+    if (__any_sync(0xffffffffu, g.bad) && lane == 0) report(status, SA_ERR_SELECTED_RANGE);
+    const volatile int64_t* pre_v = seg_pre;
+    const int64_t pre0 = pre_v[3 * my_seg + 0];
+    const int64_t pre1 = pre_v[3 * my_seg + 1];
+    const int64_t pre2 = pre_v[3 * my_seg + 2];
+    const int64_t head_edges = pre_v[3 * static_cast<int64_t>(h) * batch + 0];
+    const int64_t head_units = pre_v[3 * static_cast<int64_t>(h) * batch + 1];
+    const int64_t nbs = a.nbs;
 #pragma unroll
-      for (int j = 0; j < 3; ++j) pre[j] = *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * seg + j);
-      const int64_t head_edges =
-          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 0);
-      const int64_t head_units =
-          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch + 1);
-      // ranks among the opening entries: units and splits of smaller blocks
-      int ul[2] = {0, 0};
-      int64_t sl[2] = {0, 0};
-      for (int j = 0; j < n; ++j) {
-        const int src = j & 31;
-        const bool lo = j < 32;
-        const int xj = __shfl_sync(0xffffffffu, lo ? g.blk[0] : g.blk[1], src);
-        const int bj = __shfl_sync(0xffffffffu, lo ? g.before[0] : g.before[1], src);
-        const int sj = __shfl_sync(0xffffffffu, lo ? g.same[0] : g.same[1], src);
-        if (xj < 0 || bj != 0) continue;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (g.blk[k] >= 0 && xj < g.blk[k]) {
-            ++ul[k];
-            sl[k] += splits_of(sj, a.split_edges);
-          }
+    for (int k = 0; k < 2; ++k) {
+      const int t = 32 * k + lane;
+      if (t >= g.n) continue;
+      const int64_t i = g.q0 + t / topk;
+      const int r = t % topk;
+      const int64_t inv_at = (static_cast<int64_t>(h) * a.tq + i) * topk + r;
+      if (g.blk[k] < 0) {
+        a.idx.inv[inv_at] = -1;
+        continue;
       }
-      const int64_t q0 = a.cu[b];
-      const int64_t nbs = a.nbs;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int t = 32 * k + lane;
-        if (t >= n) continue;
-        const int64_t i = q0 + t / topk;
-        const int r = t % topk;
-        const int64_t inv_at = (static_cast<int64_t>(h) * a.tq + i) * topk + r;
-        if (g.blk[k] < 0) {
-          a.idx.inv[inv_at] = -1;
-          continue;
-        }
-        const int64_t first = pre[0] + g.less[k];          // absolute edge of the bucket
-        const int64_t pos = first + g.before[k];
-        if (pos >= 0 && pos < cap) {
-          reinterpret_cast<int2*>(a.idx.edges)[pos] = make_int2(static_cast<int32_t>(i), r);
-          a.idx.inv[inv_at] = static_cast<int32_t>(pos - head_edges);
-        }
-        if (g.before[k] != 0) continue;
-        const int64_t j = pre[1] - head_units + ul[k];
-        if (j >= 0 && j < nbs) {
-          a.idx.sel_slots[h * nbs + j] = static_cast<int32_t>(static_cast<int64_t>(b) * msb + g.blk[k]);
-          a.idx.sel_offsets[h * (nbs + 1) + j] = static_cast<int32_t>(first - head_edges);
-        }
-        const int cnt = g.same[k];
-        const int step = a.split_edges > 0 ? a.split_edges : cnt;
-        const int64_t nsp = splits_of(cnt, a.split_edges);
-        for (int64_t u = 0; u < nsp; ++u) {
-          const int64_t gs = pre[2] + sl[k] + u;
-          if (gs < cap) {
-            const int64_t lo_e = first + u * step;
-            int4 w;
-            w.x = h;
-            w.y = static_cast<int32_t>(j);
-            w.z = static_cast<int32_t>(lo_e);
-            w.w = static_cast<int32_t>(min(lo_e + step, first + cnt));
-            reinterpret_cast<int4*>(a.idx.splits)[gs] = w;
-          }
+      const int64_t first = pre0 + g.less[k];             // absolute edge of the bucket
+      const int64_t pos = first + g.before[k];
+      if (pos >= 0 && pos < cap) {
+        reinterpret_cast<int2*>(a.idx.edges)[pos] = make_int2(static_cast<int32_t>(i), r);
+        a.idx.inv[inv_at] = static_cast<int32_t>(pos - head_edges);
+      }
+      if (g.before[k] != 0) continue;
+      const int64_t j = pre1 - head_units + g.ul[k];
+      if (j >= 0 && j < nbs) {
+        a.idx.sel_slots[h * nbs + j] = static_cast<int32_t>(static_cast<int64_t>(b) * msb + g.blk[k]);
+        a.idx.sel_offsets[h * (nbs + 1) + j] = static_cast<int32_t>(first - head_edges);
+      }
+      const int cnt = g.same[k];
+      const int step = a.split_edges > 0 ? a.split_edges : cnt;
+      const int64_t nsp = splits_of(cnt, a.split_edges);
+      for (int64_t u = 0; u < nsp; ++u) {
+        const int64_t gs = pre2 + g.sl[k] + u;
+        if (gs < cap) {
+          const int64_t lo_e = first + u * step;
+          int4 w;
+          w.x = h;
+          w.y = static_cast<int32_t>(j);
+          w.z = static_cast<int32_t>(lo_e);
+          w.w = static_cast<int32_t>(min(lo_e + step, first + cnt));
+          reinterpret_cast<int4*>(a.idx.splits)[gs] = w;
         }
       }
     }
   }
-  for (int64_t c = a.small ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
+  for (int64_t c = kSmall ? n_chunks : blockIdx.x; c < n_chunks; c += gridDim.x) {
     int h, b, k;
     locate(c, chunk_base, batch, nch_head, h, b, k);
     const int nc = chunk_base[b + 1] - chunk_base[b];
@@ -672,16 +748,14 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
       a.idx.totals[2] = all[1];
     }
   }
-  const int64_t nbs = a.nbs;
-  const int64_t per_head = nbs + 1;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + tid; g < a.hkv * per_head;
-       g += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int h = static_cast<int>(g / per_head);
-    const int64_t p = g - h * per_head;
-    if (p >= head_tot[2 * h + 1]) {
-      a.idx.sel_offsets[g] = static_cast<int32_t>(head_tot[2 * h + 0]);
-      if (p < nbs) a.idx.sel_slots[h * nbs + p] = -1;
-    }
+  // Past each head's kept slots: sel_offsets (through index nbs) holds E_h,
+  // sel_slots -1.
+  for (int h = 0; h < a.hkv; ++h) {
+    const int64_t kept = head_tot[2 * h + 1];
+    fill_i32(a.idx.sel_offsets + static_cast<int64_t>(h) * (a.nbs + 1) + kept, a.nbs + 1 - kept,
+             static_cast<int32_t>(head_tot[2 * h + 0]), gtid, gthreads);
+    fill_i32(a.idx.sel_slots + static_cast<int64_t>(h) * a.nbs + kept, a.nbs - kept, -1, gtid,
+             gthreads);
   }
 }
 
@@ -750,37 +824,48 @@ cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
       workspace_layout(a.hkv, a.batch, a.tq, hist_slots_per_head, a.msb);
   cudaError_t err = cudaMemsetAsync(a.idx.workspace, 0, lay.zero_bytes, stream);
   if (err != cudaSuccess) return err;
-  const size_t smem = index_smem_bytes(a.msb, a.batch, a.hkv);
-  if (smem > 227 * 1024) return cudaErrorNotSupported;
-  if (smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-  }
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_kernel, kThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorNotSupported;
-  const int64_t n_chunks = chunks_per_head * a.hkv;
-  int64_t grid = static_cast<int64_t>(per_sm) * device_sm_count();
-  const int64_t plateau_ctas = (static_cast<int64_t>(a.hkv) * (a.nbs + 1) + kThreads - 1) / kThreads;
-  // work items: chunks, or in warp-per-segment mode warps' worth of segments
-  const int64_t items =
-      a.small ? (static_cast<int64_t>(a.hkv) * a.batch + kWarps - 1) / kWarps : n_chunks;
-  int64_t want = std::max<int64_t>(std::max<int64_t>(items, plateau_ctas), 1);
-  // warp-per-segment mode: one CTA per SM at most (a smaller barrier; the
-  // plateau is then a few dozen coalesced stores per thread)
-  if (a.small) want = std::max<int64_t>(items, std::min<int64_t>(want, device_sm_count()));
-  if (grid > want) grid = want;
   IndexArgs args = a;
+  const int sms = device_sm_count();
+  // warp-per-segment mode: a warp for every segment in one launch, one CTA
+  // per SM at most (a smaller barrier); its shared memory is the per-head
+  // totals only
+  const int64_t seg_ctas = (static_cast<int64_t>(a.hkv) * a.batch + kWarps - 1) / kWarps;
+  int per_sm = 0;
+  size_t smem = 16 * static_cast<size_t>(a.hkv);
+  if (args.small) {
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_kernel<true>, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (seg_ctas > static_cast<int64_t>(per_sm) * sms) args.small = 0;
+  }
+  const void* fn = reinterpret_cast<const void*>(index_kernel<true>);
+  int64_t grid = 0;
+  int64_t nch = 0;
+  if (args.small) {
+    grid = std::max<int64_t>(seg_ctas, std::min<int64_t>(seg_ctas * kWarps, sms));
+  } else {
+    fn = reinterpret_cast<const void*>(index_kernel<false>);
+    smem = index_smem_bytes(a.msb, a.batch, a.hkv);
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    if (smem > 48 * 1024) {
+      err = cudaFuncSetAttribute(index_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+      if (err != cudaSuccess) return err;
+    }
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_kernel<false>, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    nch = chunks_per_head * a.hkv;
+    const int64_t plateau_ctas =
+        (static_cast<int64_t>(a.hkv) * (a.nbs + 1) + 4 * kThreads - 1) / (4 * kThreads);
+    grid = std::min<int64_t>(static_cast<int64_t>(per_sm) * sms,
+                             std::max<int64_t>(std::max<int64_t>(nch, plateau_ctas), 1));
+  }
   int site = kStallNone;
   debug_stall_setting(&site, &args.spin_limit);
   args.stall = site == kStallIndexBarrier;
   WorkspaceLayout layout = lay;
-  int64_t nch = a.small ? 0 : n_chunks;
   void* params[] = {&args, &layout, &nch};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(index_kernel),
-                                     dim3(static_cast<unsigned>(grid)), dim3(kThreads), params,
+  return cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(kThreads), params,
                                      smem, stream);
 }
 
