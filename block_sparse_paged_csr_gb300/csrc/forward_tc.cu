@@ -1318,7 +1318,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap omap, ForwardArgs a) {
 // The longest-first work list: every unit (kv head, compact slot) of the
 // index, numbered across heads as the scheduler numbers them.  Cost model:
 // a unit costs about its edges (each edge is qhead rows of the tile loop);
-// a unit whose cost reaches an eighth of a CTA's mean share (E / ctas / 8
+// a unit whose cost reaches a thirty-second of a CTA's mean share (E / ctas / 32
 // edges) is heavy and could leave the SMs idle behind it if claimed late,
 // so heavy units come first, in classes of descending size (2^c <= edges <
 // 2^(c+1)); the light rest keep index order, where neighbouring blocks,
@@ -1344,7 +1344,7 @@ __device__ __forceinline__ int unit_class(const ForwardArgs& a, const int32_t* u
   return min(1 + 31 - __clz(c), kOrderClasses - 1);
 }
 
-// Edges from which a unit is heavy: an eighth of a CTA's mean share.
+// Edges from which a unit is heavy: a thirty-second of a CTA's mean share.
 __device__ __forceinline__ int64_t heavy_edges(const ForwardArgs& a) {
   const int64_t e = a.totals[0] > 0 ? a.totals[0] : 0;
   const int64_t share = e / (32 * static_cast<int64_t>(a.order_ctas > 0 ? a.order_ctas : 1));

@@ -3,7 +3,7 @@ longest-first claiming).
 
 The forward.rs page walks its WorkSplit list with a thread pool; here the
 units (kv head, block) are claimed by persistent CTAs from a counter that
-walks a list with the heavy units (an eighth of a CTA's mean share of edges
+walks a list with the heavy units (a thirty-second of a CTA's mean share of edges
 or more) first, by descending size class, and the light rest in index
 order.  On a skewed selection
 (Zipf block popularity: a few units with hundreds of edges, many with a few)
