@@ -514,9 +514,9 @@ def measure_workload(name, args, rank, world, local_rank):
         "e2e": e2e,
         # library kernels per step: the index kernel, then the fused decode
         # kernel, or forward + combine (the tensor-core forward preceded by
-        # the pass that rounds Q to bf16 into its scratch and the one that
-        # sorts its units longest-first)
-        "gpu_launches": (2 if fused else (5 if fwd_kernel == "forward_tc_kernel" else 3))
+        # the pass that rounds Q to bf16 into its scratch and the two that
+        # build its longest-first work list)
+        "gpu_launches": (2 if fused else (6 if fwd_kernel == "forward_tc_kernel" else 3))
                         * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
