@@ -104,6 +104,29 @@ __device__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t gen0, uint
   return s_ok != 0;
 }
 
+// Arrival-only grid barrier (the counter cleared before the launch): every
+// CTA adds one (acquire-release, after its writes) and waits (bounded) until
+// all have.  Nothing is computed at the barrier: the readers derive what
+// they need from the published totals themselves.
+__device__ bool grid_arrive_wait(uint32_t* count, uint32_t nblocks, uint32_t limit, bool stall) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_ok = 1;
+    if (!stall) atom_add_acq_rel_u32(count, 1u);   // test hook: nobody arrives
+    uint32_t it = 0;
+    while (ld_acquire_u32(count) < nblocks) {
+      if (++it > limit) {
+        s_ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
 // Block-wide sum of three 64-bit values; every thread gets the totals.
 __device__ __forceinline__ void block_sum3(int64_t v[3], int64_t (*scratch)[kWarps]) {
   const int lane = threadIdx.x & 31;
@@ -166,6 +189,7 @@ struct Shared {
   int32_t nmulti_head;   // histogram slots per head
   int last;
   uint32_t gen0;         // barrier generation at the start
+  int64_t my_pre[kWarps][3];  // warp-per-segment mode: the warps' segment prefixes
 };
 
 // Which (head, sequence, chunk) a chunk id names.
@@ -517,17 +541,86 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
       for (int j = 0; j < 3; ++j) seg_pre[3 * nseg + j] = tot[j];
     __threadfence();
   };
-  if (!grid_barrier(bar_count, bar_gen, s.gen0, gridDim.x, a.spin_limit ? a.spin_limit : kSpinLimit,
-                    a.stall != 0, scan_segments)) {
-    if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
-    return;
-  }
-  // Per-head totals of edges and non-empty bins.
-  for (int h = tid; h < a.hkv; h += kThreads) {
-    const volatile int64_t* lo = seg_pre + 3 * static_cast<int64_t>(h) * batch;
-    const volatile int64_t* hi = seg_pre + 3 * static_cast<int64_t>(h + 1) * batch;
-    head_tot[2 * h + 0] = hi[0] - lo[0];
-    head_tot[2 * h + 1] = hi[1] - lo[1];
+  const uint32_t limit = a.spin_limit ? a.spin_limit : kSpinLimit;
+  // head_start[h][j]: exclusive prefix of (edges, non-empty bins, splits) at
+  // head h's first segment, [hkv] the grand totals (warp-per-segment mode)
+  int64_t* head_start = head_tot + 2 * a.hkv;
+  if constexpr (kSmall) {
+    if (!grid_arrive_wait(bar_count, gridDim.x, limit, a.stall != 0)) {
+      if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    // Every CTA scans the segment totals itself (each thread loads its run
+    // of segments at once, one block scan) and keeps the prefixes it needs:
+    // its warps' segments and the heads' first segments.
+    constexpr int kKeep = 4;
+    const int per = (nseg + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, nseg);
+    const int hi = min(lo + per, nseg);
+    const volatile int32_t* tot_v = seg_tot;
+    int32_t keep[kKeep][3];
+    int64_t v[3] = {0, 0, 0};
+    if (per <= kKeep) {
+#pragma unroll
+      for (int u = 0; u < kKeep; ++u)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) keep[u][j] = lo + u < hi ? tot_v[3 * (lo + u) + j] : 0;
+#pragma unroll
+      for (int u = 0; u < kKeep; ++u)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) v[j] += keep[u][j];
+    } else {
+      for (int q = lo; q < hi; ++q)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) v[j] += tot_v[3 * q + j];
+    }
+    int64_t excl[3], tot[3];
+    block_scan3(v, excl, tot, s.scratch);
+    auto place = [&](int q) {
+      if (q % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x) &&
+          q / static_cast<int>(gridDim.x) < kWarps)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) s.my_pre[q / gridDim.x][j] = excl[j];
+      if (q % batch == 0)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) head_start[3 * (q / batch) + j] = excl[j];
+    };
+    if (per <= kKeep) {
+#pragma unroll
+      for (int u = 0; u < kKeep; ++u)
+        if (lo + u < hi) {
+          place(lo + u);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) excl[j] += keep[u][j];
+        }
+    } else {
+      for (int q = lo; q < hi; ++q) {
+        place(q);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) excl[j] += tot_v[3 * q + j];
+      }
+    }
+    if (tid == 0)
+#pragma unroll
+      for (int j = 0; j < 3; ++j) head_start[3 * a.hkv + j] = tot[j];
+    __syncthreads();
+    for (int h = tid; h < a.hkv; h += kThreads) {
+      head_tot[2 * h + 0] = head_start[3 * (h + 1) + 0] - head_start[3 * h + 0];
+      head_tot[2 * h + 1] = head_start[3 * (h + 1) + 1] - head_start[3 * h + 1];
+    }
+  } else {
+    if (!grid_barrier(bar_count, bar_gen, s.gen0, gridDim.x, limit, a.stall != 0,
+                      scan_segments)) {
+      if (tid == 0) report(status, SA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    // Per-head totals of edges and non-empty bins.
+    for (int h = tid; h < a.hkv; h += kThreads) {
+      const volatile int64_t* lo = seg_pre + 3 * static_cast<int64_t>(h) * batch;
+      const volatile int64_t* hi = seg_pre + 3 * static_cast<int64_t>(h + 1) * batch;
+      head_tot[2 * h + 0] = hi[0] - lo[0];
+      head_tot[2 * h + 1] = hi[1] - lo[1];
+    }
   }
   __syncthreads();
 
@@ -539,12 +632,11 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
     // and its work splits, placed by the buckets of smaller blocks
     const int h = my_seg / batch, b = my_seg - (my_seg / batch) * batch;
     if (__any_sync(0xffffffffu, g.bad) && lane == 0) report(status, SA_ERR_SELECTED_RANGE);
-    const volatile int64_t* pre_v = seg_pre;
-    const int64_t pre0 = pre_v[3 * my_seg + 0];
-    const int64_t pre1 = pre_v[3 * my_seg + 1];
-    const int64_t pre2 = pre_v[3 * my_seg + 2];
-    const int64_t head_edges = pre_v[3 * static_cast<int64_t>(h) * batch + 0];
-    const int64_t head_units = pre_v[3 * static_cast<int64_t>(h) * batch + 1];
+    const int64_t pre0 = s.my_pre[warp][0];
+    const int64_t pre1 = s.my_pre[warp][1];
+    const int64_t pre2 = s.my_pre[warp][2];
+    const int64_t head_edges = head_start[3 * h + 0];
+    const int64_t head_units = head_start[3 * h + 1];
     const int64_t nbs = a.nbs;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -737,15 +829,17 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   if (blockIdx.x == 0) {
     for (int h = tid; h <= a.hkv; h += kThreads) {
       a.idx.edge_head_base[h] =
-          *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch);
+          kSmall ? head_start[3 * h]
+                 : *reinterpret_cast<volatile int64_t*>(seg_pre + 3 * static_cast<int64_t>(h) * batch);
       if (h < a.hkv) a.idx.num_sel[h] = static_cast<int32_t>(head_tot[2 * h + 1]);
     }
     if (tid == 0) {
-      // totals: E, work splits, non-empty units (seg_pre holds edges, units, splits)
+      // totals: E, work splits, non-empty units (the prefixes hold edges,
+      // units, splits)
       const volatile int64_t* all = seg_pre + 3 * static_cast<int64_t>(nseg);
-      a.idx.totals[0] = all[0];
-      a.idx.totals[1] = all[2];
-      a.idx.totals[2] = all[1];
+      a.idx.totals[0] = kSmall ? head_start[3 * a.hkv + 0] : all[0];
+      a.idx.totals[1] = kSmall ? head_start[3 * a.hkv + 2] : all[2];
+      a.idx.totals[2] = kSmall ? head_start[3 * a.hkv + 1] : all[1];
     }
   }
   // Past each head's kept slots: sel_offsets (through index nbs) holds E_h,
@@ -831,7 +925,7 @@ cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
   // totals only
   const int64_t seg_ctas = (static_cast<int64_t>(a.hkv) * a.batch + kWarps - 1) / kWarps;
   int per_sm = 0;
-  size_t smem = 16 * static_cast<size_t>(a.hkv);
+  size_t smem = 16 * static_cast<size_t>(a.hkv) + 24 * (static_cast<size_t>(a.hkv) + 1);
   if (args.small) {
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_kernel<true>, kThreads, smem);
     if (err != cudaSuccess) return err;
