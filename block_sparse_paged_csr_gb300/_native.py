@@ -19,7 +19,8 @@ PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CUDA_CORE_GENERAL, PATH_FUSED_
 PATH_TENSOR_CORE_TF32 = 5
 
 #: Every symbol include/sa.h declares.
-EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_build_index",
+EXPORTS = ("sa_status_string", "sa_version", "sa_index_query_sizes", "sa_index_workspace_size",
+           "sa_build_index",
            "sa_build_index_no_alloc", "sa_forward", "sa_forward_ex", "sa_forward_combine",
            "sa_forward_combine_ex", "sa_forward_kernel_name", "sa_attention_kernel_name",
            "sa_combine", "sa_combine_ex", "sa_attention", "sa_attention_ex", "sa_get_status",
@@ -80,6 +81,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sa_index_query_sizes.argtypes = [i64, i32, i32, i32, i32, i32, i32,
                                          ctypes.POINTER(SaIndexSizes)]
     lib.sa_index_query_sizes.restype = st
+    lib.sa_index_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32, i32,
+                                            ctypes.POINTER(ctypes.c_size_t)]
+    lib.sa_index_workspace_size.restype = st
     lib.sa_build_index.argtypes = [p, i64, i32, i32, p, p, i32, p, i32, i32, i32, i32,
                                    ctypes.POINTER(SaIndex), p]
     lib.sa_build_index.restype = st

@@ -203,6 +203,18 @@ sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t ba
   return SA_OK;
 }
 
+sa_status sa_index_workspace_size(int64_t tq, int32_t hkv, int32_t topk, int32_t batch,
+                                  int32_t max_pages, int32_t block_size, int32_t page_size,
+                                  size_t* bytes) {
+  if (bytes == nullptr) return SA_ERR_INVALID_ARGUMENT;
+  sa_index_sizes z;
+  const sa_status st =
+      sa_index_query_sizes(tq, hkv, topk, batch, max_pages, block_size, page_size, &z);
+  if (st != SA_OK) return st;
+  *bytes = z.workspace_bytes;
+  return SA_OK;
+}
+
 sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32_t topk,
                          const int64_t* cu_seqlens_q_host, const int64_t* cu_seqlens_q,
                          int32_t batch, const int32_t* used_kv_lens, int32_t max_pages,

@@ -167,6 +167,16 @@ sa_status sa_index_query_sizes(int64_t tq, int32_t hkv, int32_t topk, int32_t ba
                                sa_index_sizes *out);
 
 /*
+ * The workspace size alone (sa_index_query_sizes(...)->workspace_bytes):
+ * bytes of device memory the caller hands sa_build_index in
+ * sa_index.workspace for an index of these sizes.  Same errors as
+ * sa_index_query_sizes; SA_ERR_INVALID_ARGUMENT when bytes == NULL.
+ */
+sa_status sa_index_workspace_size(int64_t tq, int32_t hkv, int32_t topk, int32_t batch,
+                                  int32_t max_pages, int32_t block_size, int32_t page_size,
+                                  size_t *bytes);
+
+/*
  * Step 1: build the KV-outer CSR index (build_kvouter_index; fields of
  * KvOuterIndex in types.rs).
  *

@@ -63,6 +63,13 @@ def test_index_sizes_of_the_serving_workloads(lib):
     # long-context decode: B=128, Hkv=8, topk=64, max_pages=8192
     assert lib.sa_index_query_sizes(128, 8, 64, 128, 8192, 64, 16, ctypes.byref(s)) == 0
     assert (s.msb, s.nbs) == (2048, 262144)
+    # the boundary's workspace-size entry gives the same bytes, and the same errors
+    n = ctypes.c_size_t(0)
+    assert lib.sa_index_workspace_size(128, 8, 64, 128, 8192, 64, 16, ctypes.byref(n)) == 0
+    assert n.value == s.workspace_bytes > 0
+    assert lib.sa_index_workspace_size(128, 8, 64, 128, 8192, 64, 16, None) != 0
+    assert (lib.sa_index_workspace_size(128, 8, 64, 128, 8192, 40, 16, ctypes.byref(n)) ==
+            lib.sa_index_query_sizes(128, 8, 64, 128, 8192, 40, 16, ctypes.byref(s)) != 0)
 
 
 def _build(lib, **kw):
