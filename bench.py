@@ -512,11 +512,12 @@ def measure_workload(name, args, rank, world, local_rank):
                                                        "step", "forward", "combine")},
         "edges": acct["edges"],
         "e2e": e2e,
-        # library kernels per step: the index kernel, then the fused decode
-        # kernel, or forward + combine (the tensor-core forward preceded by
-        # the pass that rounds Q to bf16 into its scratch and the two that
-        # build its longest-first work list)
-        "gpu_launches": (2 if fused else (6 if fwd_kernel == "forward_tc_kernel" else 3))
+        # library kernels per step: on the fused decode path the clear of the
+        # build's counters, then the index kernel beside the fused decode
+        # kernel; otherwise the index kernel, forward and combine (the
+        # tensor-core forward preceded by the pass that rounds Q to bf16 into
+        # its scratch and the two that build its longest-first work list)
+        "gpu_launches": (3 if fused else (6 if fwd_kernel == "forward_tc_kernel" else 3))
                         * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,

@@ -215,11 +215,47 @@ sa_status sa_index_workspace_size(int64_t tq, int32_t hkv, int32_t topk, int32_t
   return SA_OK;
 }
 
-sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32_t topk,
-                         const int64_t* cu_seqlens_q_host, const int64_t* cu_seqlens_q,
-                         int32_t batch, const int32_t* used_kv_lens, int32_t max_pages,
-                         int32_t block_size, int32_t page_size, int32_t split_edges,
-                         sa_index* idx, void* stream) {
+namespace {
+
+// Per host thread and device: the side stream an index build runs on beside
+// the fused decode kernel (sa_attention), and the events of the fork and the
+// join.  Created on first use; none (the build then runs in stream order)
+// where creation fails.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false, ok = false;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_device[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  SideStream& r = per_device[dev];
+  if (!r.tried) {
+    r.tried = true;
+    r.ok = cudaStreamCreateWithFlags(&r.s, cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!r.ok) cudaGetLastError();
+  }
+  return r.ok ? &r : nullptr;
+}
+
+// Step 1.  With `side`: the workspace counters and the status word are
+// cleared on `stream`, then the build runs on the side stream, forked from
+// `stream` (the caller joins it back after launching what runs beside it).
+sa_status build_index_impl(const int32_t* selected, int64_t tq, int32_t hkv, int32_t topk,
+                           const int64_t* cu_seqlens_q_host, const int64_t* cu_seqlens_q,
+                           int32_t batch, const int32_t* used_kv_lens, int32_t max_pages,
+                           int32_t block_size, int32_t page_size, int32_t split_edges,
+                           sa_index* idx, void* stream, SideStream* side,
+                           bool* forked = nullptr) {
+  if (forked != nullptr) *forked = false;
   if (block_size <= 0 || page_size <= 0 || block_size % page_size != 0) return SA_ERR_BLOCK_PAGE;
   if (tq == 0 || hkv == 0 || topk == 0) return SA_ERR_EMPTY;
   sa_status st = validate_cu_host(cu_seqlens_q_host, batch);
@@ -275,10 +311,32 @@ sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32
   for (int32_t b = 0; b < batch; ++b)
     longest = std::max<int64_t>(longest, cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b]);
   a.small = longest * topk <= sa::kSmallSegment ? 1 : 0;
-  const cudaError_t err =
-      sa::launch_build_index(a, chunks_per_head, multi_slots, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (side != nullptr) {
+    if (sa::launch_clear_for_build(idx->workspace, lay.zero_bytes, idx->totals + 3, s) !=
+            cudaSuccess ||
+        cudaEventRecord(side->fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return SA_ERR_CUDA;
+    if (forked != nullptr) *forked = true;
+    a.external_clear = 1;
+    s = side->s;
+  }
+  const cudaError_t err = sa::launch_build_index(a, chunks_per_head, multi_slots, s);
   if (err == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
   return err == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+}  // namespace
+
+sa_status sa_build_index(const int32_t* selected, int64_t tq, int32_t hkv, int32_t topk,
+                         const int64_t* cu_seqlens_q_host, const int64_t* cu_seqlens_q,
+                         int32_t batch, const int32_t* used_kv_lens, int32_t max_pages,
+                         int32_t block_size, int32_t page_size, int32_t split_edges,
+                         sa_index* idx, void* stream) {
+  return build_index_impl(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q, batch,
+                          used_kv_lens, max_pages, block_size, page_size, split_edges, idx,
+                          stream, nullptr);
 }
 
 namespace {
@@ -705,15 +763,28 @@ sa_status sa_attention_ex(const float* q, const void* k_pages, const void* v_pag
       !((path == SA_PATH_TENSOR_CORE || path == SA_PATH_TENSOR_CORE_TF32) &&
         sa::forward_tc_supported(head_dim, block_size, page_size, hq / hkv)))
     return SA_ERR_UNSUPPORTED;
-  const sa_status st = sa_build_index(selected, tq, hkv, topk, cu_seqlens_q_host, cu_seqlens_q,
-                                      batch, used_kv_lens, max_pages, block_size, page_size,
-                                      split_edges, idx, stream);
-  if (st != SA_OK) return st;
-  return forward_combine_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
-                              cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
-                              head_dim, block_size, page_size, softmax_scale, causal, split_edges,
-                              partial_dtype, o_partial, m_partial, l_partial, out, lse, path,
-                              stream, true);
+  // The fused decode kernel reads no output of the index build: the build
+  // runs beside it on a side stream (both after the workspace counters and
+  // the status word are cleared in stream order), joined back before the
+  // call returns, so later work on `stream` sees both complete.  Without a
+  // side stream the fused kernel is the build's programmatic dependent.
+  SideStream* side = fused ? side_stream() : nullptr;
+  bool forked = false;
+  const sa_status st = build_index_impl(selected, tq, hkv, topk, cu_seqlens_q_host,
+                                        cu_seqlens_q, batch, used_kv_lens, max_pages, block_size,
+                                        page_size, split_edges, idx, stream, side, &forked);
+  sa_status st2 = st;
+  if (st == SA_OK)
+    st2 = forward_combine_impl(q, k_pages, v_pages, num_pages, kv_dtype, idx, selected,
+                               cu_seqlens_q_host, cu_seqlens_q, used_kv_lens, block_tables, hq,
+                               head_dim, block_size, page_size, softmax_scale, causal,
+                               split_edges, partial_dtype, o_partial, m_partial, l_partial, out,
+                               lse, path, stream, side == nullptr);
+  if (forked && (cudaEventRecord(side->join, side->s) != cudaSuccess ||
+                          cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), side->join, 0) !=
+                              cudaSuccess))
+    return SA_ERR_CUDA;
+  return st2;
 }
 
 sa_status sa_attention(const float* q, const void* k_pages, const void* v_pages,

@@ -317,7 +317,7 @@ __device__ __forceinline__ void fill_i32(int32_t* p, int64_t n, int32_t v, int64
 }
 
 template <bool kSmall>
-__global__ void __launch_bounds__(kThreads, kSmall ? 2 : 4)
+__global__ void __launch_bounds__(kThreads, 4)
 index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
   extern __shared__ int64_t dyn64[];
   const int msb = a.msb;
@@ -378,7 +378,7 @@ index_kernel(IndexArgs a, WorkspaceLayout lay, int64_t n_chunks) {
     }
   }
   if (tid == 0) s.gen0 = ld_acquire_u32(bar_gen);
-  if (blockIdx.x == 0 && tid == 0) {
+  if (blockIdx.x == 0 && tid == 0 && !a.external_clear) {
     *status = 0;
     __threadfence();
   }
@@ -912,12 +912,34 @@ LptRegion lpt_region(int64_t tq, int32_t hkv, int32_t topk, int32_t batch, int32
   return r;
 }
 
+namespace {
+// The workspace counters and the status word cleared in one launch (for a
+// build that runs beside a fused decode kernel: both start from them).
+__global__ void __launch_bounds__(256) clear_kernel(uint4* ws, int64_t n16, int64_t* status) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i < n16) ws[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (i == 0) *status = 0;
+}
+}  // namespace
+
+cudaError_t launch_clear_for_build(void* workspace, size_t bytes, int64_t* status,
+                                   cudaStream_t stream) {
+  const int64_t n16 = static_cast<int64_t>(bytes / 16);
+  const int64_t grid = (n16 + 255) / 256;
+  clear_kernel<<<static_cast<unsigned>(grid > 0 ? grid : 1), 256, 0, stream>>>(
+      static_cast<uint4*>(workspace), n16, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
                                int64_t hist_slots_per_head, cudaStream_t stream) {
   const WorkspaceLayout lay =
       workspace_layout(a.hkv, a.batch, a.tq, hist_slots_per_head, a.msb);
-  cudaError_t err = cudaMemsetAsync(a.idx.workspace, 0, lay.zero_bytes, stream);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!a.external_clear) {
+    err = cudaMemsetAsync(a.idx.workspace, 0, lay.zero_bytes, stream);
+    if (err != cudaSuccess) return err;
+  }
   IndexArgs args = a;
   const int sms = device_sm_count();
   // warp-per-segment mode: a warp for every segment in one launch, one CTA

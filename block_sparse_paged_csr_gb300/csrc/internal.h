@@ -67,6 +67,10 @@ struct IndexArgs {
   int stall;                // test hook: the grid barrier is never released
   int small;                // every segment holds at most kSmallSegment entries
                             // (decode batches): one warp per segment
+  int external_clear;       // the workspace counters and the status word were
+                            // cleared by the caller, on the stream this build
+                            // waits on (the build runs beside a fused decode
+                            // kernel that may already report into the status)
 };
 
 // Largest segment (entries of one (kv head, sequence)) of the index kernel's
@@ -75,6 +79,11 @@ constexpr int kSmallSegment = 64;
 
 cudaError_t launch_build_index(const IndexArgs& a, int64_t chunks_per_head,
                                int64_t hist_slots_per_head, cudaStream_t stream);
+
+// Clears `bytes` (a multiple of 16) of a 16-byte-aligned workspace and the
+// status word in one launch.
+cudaError_t launch_clear_for_build(void* workspace, size_t bytes, int64_t* status,
+                                   cudaStream_t stream);
 
 struct ForwardArgs {
   const float* q;
