@@ -10,12 +10,17 @@
  *      kvouter_forward / process_work_unit
  *   3. sa_combine:     merge each (query, q-head)'s partials with the
  *      log-sum-exp rule                              - forward.rs, module doc
- * sa_attention runs the three in sequence on one stream with no host sync;
- * sa_forward_combine runs steps 2 and 3 on a built index.
+ * sa_attention runs the three in order on the caller's stream with no host
+ * sync (on the fused decode path the build runs beside the fused kernel on a
+ * side stream, joined back before the call returns); sa_forward_combine runs
+ * steps 2 and 3 on a built index.
  *
  * Conventions for every entry point:
  *   - Array arguments are DEVICE pointers unless the name ends in _host.  The
- *     caller owns and allocates every buffer; the library allocates nothing.
+ *     caller owns and allocates every buffer; the library allocates no device
+ *     memory (it creates one side stream and two events per host thread and
+ *     device, on the first sa_attention call that takes the fused decode
+ *     path, and keeps them for the life of the process).
  *   - Layouts are row-major and contiguous; shapes are given in brackets.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work; they return after host-side checks.
@@ -436,7 +441,14 @@ sa_status sa_combine_ex(const sa_index *idx, sa_dtype partial_dtype, const void 
  * array for an index with SA_INDEX_STATIC_SCRATCH) and the kernel leaves at
  * zero: sa_forward_combine on this path returns SA_ERR_INVALID_ARGUMENT when
  * that scratch is missing or smaller than the build's layout.  out and lse
- * equal those of the unfused path up to rounding.
+ * equal those of the unfused path up to rounding.  On this path
+ * sa_attention clears the build's counters and the status word in one launch
+ * on `stream`, then runs the index build on its side stream (forked from
+ * `stream` after the clear) while the fused kernel runs on `stream` (it reads
+ * no output of the build), and makes `stream` wait for the build before it
+ * returns: work enqueued on `stream` afterwards sees both, and a CUDA graph
+ * captured from `stream` holds the fork and the join.  An error either kernel
+ * reports stays in the status word.
  */
 sa_status sa_attention(const float *q, const void *k_pages, const void *v_pages,
                        int64_t num_pages, sa_dtype kv_dtype, const int32_t *selected,
