@@ -87,7 +87,7 @@ template <bool kBf16> struct Cfg;
 // NC consumer warps (keys of a stage split between them), NL load warps
 // (stages round-robin: one warp's copy issue alone does not keep HBM busy).
 template <> struct Cfg<false> { static constexpr int NC = 8, NL = 2; };   // 8 keys per consumer
-template <> struct Cfg<true> { static constexpr int NC = 4, NL = 2; };    // 16 keys per consumer
+template <> struct Cfg<true> { static constexpr int NC = 4, NL = 3; };    // 16 keys per consumer
 
 struct Layout {
   uint32_t tensor;     // bytes of K (or V) of one stage
